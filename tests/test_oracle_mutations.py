@@ -1,0 +1,60 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins catch
+each one.  The copy is compiled into a temporary library; the real oracle source
+is never changed."""
+import ctypes
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+MUTATIONS = {
+    "sign of q - z": ("return (float)(q - z) * s;", "return (float)(z - q) * s;"),
+    "zero point dropped": ("int z = zeros[gi];", "int z = 0;"),
+    "nibble order reversed": ("(word >> (4 * (k % 8)))", "(word >> (4 * (7 - k % 8)))"),
+    "x index reversed": ("x[(size_t)m * K + k]", "x[(size_t)m * K + (K - 1 - k)]"),
+    "half exponent bias": ("e - 25", "e - 24"),
+    "group index uses row stride K": ("(size_t)n * (size_t)G + (size_t)(k / W4O_GROUP)",
+                                      "(size_t)(k / W4O_GROUP) * (size_t)G + (size_t)n % G"),
+}
+
+PIN_CHECKS = [
+    pins.test_golden_nibble_order,
+    pins.test_golden_group_index,
+    pins.test_golden_dequant_rounding,
+    lambda: pins.test_bruteforce_exact(2, 256, 3, 1),
+    pins.test_one_hot_x_exact,
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    old, new = MUTATIONS[name]
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "w4_oracle.c")).read()
+    assert old in src, "mutation site moved"
+    path = tmp_path / "mut.c"
+    path.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libmut.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-o", str(so), str(path), "-lm"], check=True)
+    saved_lib, saved_path = oracle._lib, oracle._LIB_PATH
+    try:
+        oracle._lib = None
+        oracle._LIB_PATH = str(so)
+        oracle.build = lambda force=False, _p=str(so): _p  # noqa: E731 -- load the mutant
+        caught = 0
+        for check in PIN_CHECKS:
+            try:
+                check()
+            except AssertionError:
+                caught += 1
+        assert caught > 0, f"no pin caught mutation: {name}"
+    finally:
+        oracle._lib, oracle._LIB_PATH = saved_lib, saved_path
+        import importlib
+        importlib.reload(oracle)
