@@ -1,0 +1,463 @@
+"""Benchmark: W4 (INT4 weight-only, group 128) GEMV on one GB300.
+
+Workload (one step = one token of single-request decode through the GEMVs of a
+7B-shape model): the 28-layer chain of the four W4 GEMVs of a decoder layer
+with hidden 3584 and intermediate 18944 -- qkv 3584->4608, o 3584->3584,
+gate_up 3584->37888, down 18944->3584 -- at M = 1, 112 distinct weights
+(3.42 GB in the canonical format), captured once in a CUDA graph and replayed.
+The weights (3.4 GB) are far larger than L2 (129 MB), so every step streams
+them from HBM.
+
+Reported: effective HBM GB/s = canonical bytes per step (packed weights +
+fp16 scales + uint8 zeros + bf16 x + bf16 y) / device time, tok/s, the
+roofline of the dominant kernel (the gate_up GEMV), the end-to-end number
+through the public API with host buffers, and the CPU oracle on a bounded
+sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl w4|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from int4_weight_only_w4_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "W4g128 GEMV effective HBM GB/s and % of GB300 peak at M=1; layer-chain tok/s"
+WORKLOAD = "qwen7b-shape 28-layer W4 GEMV chain, M=1, CUDA-graph replay"
+SEED = 0
+SCALES = (0.001, 0.02)
+
+
+def canonical_bytes(M: int, K: int, N: int) -> int:
+    """Algorithmic bytes of one call: packed weights + fp16 scales + uint8 zeros
+    + bf16 x + bf16 y."""
+    G = K // 128
+    return N * K // 2 + 2 * N * G + N * G + 2 * M * K + 2 * M * N
+
+
+def chain_bytes(layers: int = syn.LAYERS_7B, M: int = 1) -> int:
+    return layers * sum(canonical_bytes(M, K, N) for _, K, N in syn.LAYER_7B)
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---- clocks during the timed region -------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- the CPU oracle on a bounded sample ----------------------------------------------
+
+class OracleSampler:
+    """Runs the CPU oracle over the chain's GEMVs in chain order (layer 0 qkv,
+    o, gate_up, down, layer 1 ...), timing only the oracle call."""
+
+    def __init__(self):
+        self.pos = 0
+
+    def next_gemv(self):
+        import oracle
+        layer, j = divmod(self.pos, len(syn.LAYER_7B))
+        kind, K, N = syn.LAYER_7B[j]
+        self.pos = (self.pos + 1) % (syn.LAYERS_7B * len(syn.LAYER_7B))
+        qw, sc, zp = syn.make_weights(f"chain7b.L{layer}.{kind}", K, N, SEED, SCALES)
+        x = syn.make_x(f"chain7b.x.{kind}", 1, K, SEED)
+        t0 = time.perf_counter()
+        oracle.gemv_f64(qw, sc, zp, x, 1, K, N)
+        return canonical_bytes(1, K, N), time.perf_counter() - t0
+
+    def run(self, seconds: float):
+        """At least one GEMV; stops once ``seconds`` of oracle time are spent."""
+        nbytes, spent, n = 0, 0.0, 0
+        while n == 0 or spent < seconds:
+            b, t = self.next_gemv()
+            nbytes, spent, n = nbytes + b, spent + t, n + 1
+        return nbytes, spent, n
+
+
+def cpu_baseline(seconds: float = 10.0):
+    b, t, n = OracleSampler().run(seconds)
+    return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n} GEMVs of the chain in order (layer 0 qkv, o, gate_up, "
+                      f"down, ...), M=1, single-threaded fp64 oracle, {t:.1f} s of compute"}
+
+
+# ---- distributed plumbing -----------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    total_bytes, total_t = 0, 0.0
+    sampler = OracleSampler()
+    for step in range(args.warmup + args.steps):
+        b, t = sampler.next_gemv()          # one GEMV per step, in chain order
+        if step >= args.warmup:
+            total_bytes += b
+            total_t += t
+    value = total_bytes / total_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total_t / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": 1, "layers": syn.LAYERS_7B,
+                   "sample_per_step": "one GEMV of the chain (layer 0 qkv first)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "one GEMV of the chain per step, single-threaded fp64 oracle"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- the GPU arm ------------------------------------------------------------------------------
+
+def build_chain(w4, torch, dev):
+    """Host-generated canonical weights -> device -> kernel layout."""
+    packed, xs, ys = [], {}, []
+    for kind, K, N in syn.LAYER_7B:
+        xs[kind] = torch.from_numpy(syn.make_x(f"chain7b.x.{kind}", 1, K, SEED).view(np.int16)) \
+            .to(dev).view(torch.bfloat16)
+    for layer in range(syn.LAYERS_7B):
+        for kind, K, N in syn.LAYER_7B:
+            qw, sc, zp = syn.make_weights(f"chain7b.L{layer}.{kind}", K, N, SEED, SCALES)
+            tq = torch.from_numpy(qw.view(np.int32)).to(dev)
+            ts = torch.from_numpy(sc.view(np.int16)).to(dev)
+            tz = torch.from_numpy(zp).to(dev)
+            packed.append((kind, w4.pack(tq, ts, tz, K, N)))
+            ys.append(torch.empty((1, N), dtype=torch.bfloat16, device=dev))
+            del tq, ts, tz
+    return packed, xs, ys
+
+
+def gpu_arm(args):
+    import torch
+    import torch.distributed as dist
+
+    from int4_weight_only_w4_gb300 import w4
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    packed, xs, ys = build_chain(w4, torch, dev)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+
+    def chain_calls():
+        for (kind, pw), y in zip(packed, ys):
+            pw.gemv(xs[kind], y, stream=stream)
+
+    # capture the whole chain once
+    with torch.cuda.stream(stream):
+        chain_calls()                    # warm-up outside capture
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        chain_calls()
+    launches_per_step = len(packed)
+
+    # dominant kernel: the 28 gate_up GEMVs back to back in one graph
+    gu = [(pw, y) for (kind, pw), y in zip(packed, ys) if kind == "gate_up"]
+    gu_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gu_graph, stream=stream):
+        for pw, y in gu:
+            pw.gemv(xs["gate_up"], y, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+            gu_graph.replay()
+    stream.synchronize()
+
+    # timed region: exactly K chain replays
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            ev1.record(stream)
+        ev1.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+        # roofline measurement of the dominant kernel (same stream)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        reps = max(3, args.steps // 4)
+        with torch.cuda.stream(stream):
+            g0.record(stream)
+            for _ in range(reps):
+                gu_graph.replay()
+            g1.record(stream)
+        g1.synchronize()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    gu_launch_us = 1e3 * g0.elapsed_time(g1) / (reps * len(gu))
+
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the public API: pinned host x in, device chain, host y out
+    h_x = {k: v.cpu().pin_memory() for k, v in xs.items()}
+    h_y = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in ys[-4:]]
+    h2d = sum(v.numel() * v.element_size() for v in h_x.values())
+    d2h = sum(v.numel() * v.element_size() for v in h_y)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, args.steps)
+    barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for k, v in h_x.items():
+                xs[k].copy_(v, non_blocking=True)
+            graph.replay()
+            for hy, y in zip(h_y, ys[-4:]):
+                hy.copy_(y, non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    t_host = (time.perf_counter() - t_host0) / e2e_steps
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    bytes_step = chain_bytes()
+    peak, peak_kind = read_peaks()
+    value = world * bytes_step / (ms * 1e-3) / 1e9
+    gu_bytes = canonical_bytes(1, 3584, 37888)
+    achieved = gu_bytes / (gu_launch_us * 1e-6) / 1e9
+    result = None
+    if rank == 0:
+        clk = clocks.summary()
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": 1, "layers": syn.LAYERS_7B,
+                       "gemvs_per_step": launches_per_step,
+                       "bytes_per_step": bytes_step, "l2": "inputs larger than L2 (3.42 GB)",
+                       "parallelism": f"replicas x{world}"},
+            "tok_per_s": round(world * 1e3 / ms, 2),
+            "frac_of_peak": round(value / world / peak, 4),
+            "peak_hbm_gbs": peak, "peak_kind": peak_kind,
+            "frac_of_nominal_8tbs": round(value / world / 8000.0, 4),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": "w4 gemv, gate_up 3584->37888, M=1",
+                         "bytes_per_launch": gu_bytes,
+                         "launch_us": round(gu_launch_us, 3), "peak_kind": peak_kind},
+            "e2e": {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 5), "host_ms_per_step": round(1e3 * t_host, 5)},
+            "gpu_launches": args.steps * launches_per_step,
+            "clocks": clk,
+        }
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+def per_shape_arm(args):
+    """Per-call timing of every workload shape: R calls over rotating weight
+    copies (so that the weights never sit in L2) captured in one CUDA graph.
+    Prints one JSON line per (shape, M)."""
+    import torch
+
+    from int4_weight_only_w4_gb300 import w4
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    peak, peak_kind = read_peaks()
+    names = [args.kernel_case] if args.kernel_case else [s[0] for s in syn.SHAPES]
+    stream = torch.cuda.Stream(device=dev)
+    for name in names:
+        _, K, N, Ms, srange = syn.shape(name)
+        qb, sb, zb = w4.repacked_sizes(K, N)
+        copies = min(4096, max(2, -(-3 * l2 // (qb + sb + zb)) + 1))
+        if args.kernel_case:
+            copies = 1                      # one weight, for profiler captures
+        qw, sc, zp = syn.make_weights(name, K, N, SEED, srange)
+        tq = torch.from_numpy(qw.view(np.int32)).to(dev)
+        ts = torch.from_numpy(sc.view(np.int16)).to(dev)
+        tz = torch.from_numpy(zp).to(dev)
+        base = w4.pack(tq, ts, tz, K, N)
+        packs = [base] + [w4.PackedWeight(K, N, base.qweight.clone(), base.scales.clone(),
+                                          base.zeros.clone()) for _ in range(copies - 1)]
+        for M in Ms:
+            x = torch.from_numpy(syn.make_x(f"{name}.M{M}", M, K, SEED).view(np.int16)) \
+                .to(dev).view(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            if args.kernel_case:
+                with torch.cuda.stream(stream):
+                    for _ in range(args.warmup + args.steps):
+                        base.gemv(x, y, stream=stream)
+                stream.synchronize()
+                print(json.dumps({"kernel_case": name, "M": M, "K": K, "N": N}), flush=True)
+                continue
+            reps = max(1, -(-64 // copies)) * copies
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                for pw in packs[:2]:
+                    pw.gemv(x, y, stream=stream)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(reps):
+                    packs[i % copies].gemv(x, y, stream=stream)
+            times = []
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    g.replay()
+                for _ in range(5):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                    e1.synchronize()
+                    times.append(e0.elapsed_time(e1) * 1e3 / reps)
+            us = statistics.median(times)
+            # eager single call (includes launch overhead through the binding)
+            t0 = time.perf_counter()
+            for _ in range(20):
+                base.gemv(x, y, stream=stream)
+            stream.synchronize()
+            eager_us = (time.perf_counter() - t0) / 20 * 1e6
+            b = canonical_bytes(M, K, N)
+            print(json.dumps({"shape": name, "M": M, "K": K, "N": N, "us_per_call": round(us, 3),
+                              "GBps": round(b / us / 1e3, 1),
+                              "frac_of_peak": round(b / us / 1e3 / peak, 4),
+                              "peak_kind": peak_kind, "bytes": b, "copies": copies,
+                              "calls_per_graph": reps, "splits": w4.gemv_config(K, N)[1],
+                              "eager_us_per_call": round(eager_us, 2),
+                              "runs_us": [round(t, 3) for t in times]}), flush=True)
+        del packs, base, tq, ts, tz
+        torch.cuda.empty_cache()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["w4", "reference"], default="w4")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--per-shape", action="store_true",
+                    help="per-call timing of every workload shape instead of the chain")
+    ap.add_argument("--kernel-case", default=None,
+                    help="run only this shape's GEMV warmup+steps times (for profilers)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return reference_arm(args)
+    if args.per_shape or args.kernel_case:
+        return per_shape_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

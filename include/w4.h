@@ -1,0 +1,164 @@
+/*
+ * w4.h -- C ABI of libw4: weight-only INT4 (group 128) matrix-vector product
+ * y = W x on one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed.  W is N x K.  Each weight is stored as a 4-bit unsigned
+ * integer q in 0..15; every group of 128 consecutive weights of a row along K
+ * has one fp16 scale s and one zero point z in 0..15, and the weight's value is
+ * w = (q - z) * s.  Activations x are bfloat16, M = 1..8 token rows; the
+ * product is y[m][n] = sum_k w[n][k] * x[m][k], accumulated in fp32.
+ *   Sources (page title, section): group-wise INT4 weights with one fp16 scale
+ *   per 128 weights of an output row -- "Building an LLM Inference Runtime: A
+ *   Deep Dive into Qwen2.5-Coder-7B on NVIDIA H100", section "The Stack
+ *   Architecture: A One-Page Overview"; a zero point per group applied as
+ *   (q - z) * s -- "Custom AWQ Dequantization Kernel", section "Dead ends in
+ *   profiling"; dequantisation fused into the matrix-vector kernel, no fp16 W
+ *   materialised -- "CodeAlign-Runtime", section "Level 3 -- INT4 Quantization
+ *   + Fused Kernel"; 1..8 rows (plain decode and a speculative-verify batch)
+ *   with identical per-row results -- "qengine", section "How it works".
+ *
+ * Canonical layout (what callers hold; row-major, contiguous):
+ *   qweight uint32 [N][K/8]: nibble j (bits 4j..4j+3) of word w is k = 8w + j
+ *   scales  uint16 [N][K/128]: binary16 bit patterns
+ *   zeros   uint8  [N][K/128]: values 0..15
+ *   x       uint16 [M][K]: bfloat16 bit patterns
+ *   y       uint16 [M][N] (bfloat16, round-to-nearest-even) or float [M][N]
+ *
+ * Conventions for every call:
+ *   - Pointers named device are CUDA device pointers; the caller owns all
+ *     memory.  The library never allocates device or pinned memory.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and is asynchronous unless stated otherwise.
+ *   - Errors are returned, never aborted on.  Argument checks happen on the
+ *     host before anything is enqueued; a failed launch returns W4_ERR_CUDA.
+ *   - K must be a positive multiple of 128, N positive, 1 <= M <= 8.
+ */
+#ifndef W4_H
+#define W4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* The same object as cudaStream_t. */
+typedef struct CUstream_st *w4_stream_t;
+
+typedef enum w4_status {
+    W4_OK = 0,
+    W4_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, zero point > 15 */
+    W4_ERR_UNSUPPORTED = 2,   /* M outside 1..8, or a call not allowed in stream capture */
+    W4_ERR_LAYOUT = 3,        /* repacked buffer header does not match */
+    W4_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
+} w4_status;
+
+#define W4_GROUP_SIZE 128
+#define W4_MAX_TOKENS 8
+#define W4_LAYOUT_ID 1
+#define W4_LAYOUT_VERSION 1
+#define W4_HEADER_BYTES 128
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *w4_status_string(w4_status status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int w4_version(void);
+
+/*
+ * Sizes in bytes of the three buffers that w4_repack writes for an N x K
+ * weight (the kernel layout).  The qweight buffer starts with a
+ * W4_HEADER_BYTES header (layout id, version, K, N).  Rows are padded to a
+ * multiple of 16 inside the buffers; the padding is never read back as output.
+ * Errors: W4_ERR_INVALID_ARG for bad K/N or a NULL output pointer.
+ */
+w4_status w4_repacked_sizes(int K, int N, size_t *qweight_bytes,
+                            size_t *scales_bytes, size_t *zeros_bytes);
+
+/*
+ * Offline, once per weight matrix: canonical layout -> kernel layout.
+ * The offline packing step of "Building an LLM Inference Runtime ...",
+ * sections "The Stack Architecture" and "Bug #3" (the runtime consumes one
+ * fixed nibble interleave and refuses any other layout id).
+ *
+ *   qweight, scales, zeros : device, canonical layout (see top); qweight 16-byte
+ *                            aligned, scales 2-byte aligned
+ *   qweight_out, scales_out, zeros_out : device, sizes from w4_repacked_sizes;
+ *                            qweight_out and scales_out 16-byte aligned
+ *
+ * Validates every zero point on the device (must be <= 15) and therefore
+ * synchronises `stream` before returning: not capturable into a CUDA graph
+ * (returns W4_ERR_UNSUPPORTED if `stream` is capturing).
+ * Errors: W4_ERR_INVALID_ARG (bad sizes/pointers, or a zero point > 15 -- the
+ * outputs are then unspecified), W4_ERR_CUDA.
+ */
+w4_status w4_repack(const uint32_t *qweight, const uint16_t *scales,
+                    const uint8_t *zeros, int K, int N, void *qweight_out,
+                    void *scales_out, void *zeros_out, w4_stream_t stream);
+
+/*
+ * Host-side check of a repacked qweight buffer's header.  `header` is a host
+ * copy of its first W4_HEADER_BYTES bytes.  Returns W4_OK when the magic,
+ * layout id and version are this library's and K, N match; W4_ERR_LAYOUT
+ * otherwise; W4_ERR_INVALID_ARG for a NULL pointer.
+ */
+w4_status w4_check_header(const void *header, int K, int N);
+
+/*
+ * Weights to fp16, for checking: w_out[n][k] = fp16((q - z) * s), the exact
+ * product rounded once to nearest-even.  Takes the canonical layout.
+ * The "one thread per packed word, read once, unpack all eight" dequantiser of
+ * "Custom AWQ Dequantization Kernel", section "Kernel versions" (v2).
+ *
+ *   qweight, scales, zeros : device, canonical; qweight 16-byte aligned
+ *   w_out                  : device, uint16 [N][K] binary16 bits, 16-byte aligned
+ * Errors: W4_ERR_INVALID_ARG, W4_ERR_CUDA.  Zero points > 15 are used as given.
+ */
+w4_status w4_dequant(const uint32_t *qweight, const uint16_t *scales,
+                     const uint8_t *zeros, int K, int N, uint16_t *w_out,
+                     w4_stream_t stream);
+
+/*
+ * The hot path: y = W x with W in the kernel layout written by w4_repack.
+ * Dequantisation happens in registers; fp32 accumulation; deterministic (the
+ * same inputs give bit-identical y on every call) and batch-invariant (row m
+ * of y does not depend on M or on the other rows of x).  Graph-capturable:
+ * no synchronisation, allocation or host read.
+ * Fused dequantise-and-multiply GEMV of "CodeAlign-Runtime", section "Level 3",
+ * and "qengine", section "How it works" (4-bit matrix-vector kernel, partial
+ * sums added in a fixed order).
+ *
+ *   qweight, scales, zeros : device, the three buffers of w4_repack; qweight
+ *                            16-byte aligned, scales 4-byte aligned
+ *   x                      : device, bfloat16 [M][K], 4-byte aligned
+ *   y                      : device, bfloat16 [M][N], 2-byte aligned
+ * The header is not read here (that would need a device read); check it once
+ * with w4_check_header.
+ * Errors: W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED (M outside 1..8), W4_ERR_CUDA.
+ */
+w4_status w4_gemv(const void *qweight, const void *scales, const void *zeros,
+                  const uint16_t *x, uint16_t *y, int M, int K, int N,
+                  w4_stream_t stream);
+
+/* Same as w4_gemv but writes the fp32 result before the bfloat16 cast
+ * (y: device float [M][N], 4-byte aligned).  For checking. */
+w4_status w4_gemv_f32(const void *qweight, const void *scales, const void *zeros,
+                      const uint16_t *x, float *y, int M, int K, int N,
+                      w4_stream_t stream);
+
+/*
+ * The launch shape w4_gemv uses for an N x K weight on the current device:
+ * 16-row tiles per thread block and the number of K splits (thread blocks of
+ * one cluster that each reduce a slice of K and combine in a fixed order).
+ * Depends on K and N only, never on M.  Outputs may be NULL.
+ * Errors: W4_ERR_INVALID_ARG, W4_ERR_CUDA (no device).
+ */
+w4_status w4_gemv_config(int K, int N, int *tiles_per_block, int *k_splits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4_H */

@@ -1,0 +1,136 @@
+// C ABI of libw4 (declared in include/w4.h): argument checks on the host,
+// then the launches.  Nothing here allocates device or pinned memory.
+#include <string.h>
+
+#include "w4_internal.cuh"
+
+namespace {
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool valid_kn(int K, int N) { return K > 0 && K % w4::kGroup == 0 && N > 0; }
+
+w4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W4_OK : W4_ERR_CUDA; }
+
+int device_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return -1;
+    if (dev >= 0 && dev < 64) cached[dev] = sms;
+    return sms;
+}
+
+w4_status gemv_common(const void *qweight, const void *scales, const void *zeros,
+                      const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
+                      w4_stream_t stream) {
+    if (!qweight || !scales || !zeros || !x || !y) return W4_ERR_INVALID_ARG;
+    if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
+    if (M < 1 || M > W4_MAX_TOKENS) return W4_ERR_UNSUPPORTED;
+    if (!aligned(qweight, 16) || !aligned(scales, 4) || !aligned(x, 4) ||
+        !aligned(y, f32_out ? 4 : 2))
+        return W4_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return W4_ERR_CUDA;
+    w4::GemvShape shape;
+    if (!w4::gemv_shape(K, N, sms, &shape)) return W4_ERR_UNSUPPORTED;
+    return cuda_status(w4::launch_gemv(qweight, scales, zeros, x, y, f32_out, M, K, N, shape,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *w4_status_string(w4_status status) {
+    switch (status) {
+        case W4_OK: return "W4_OK";
+        case W4_ERR_INVALID_ARG: return "W4_ERR_INVALID_ARG";
+        case W4_ERR_UNSUPPORTED: return "W4_ERR_UNSUPPORTED";
+        case W4_ERR_LAYOUT: return "W4_ERR_LAYOUT";
+        case W4_ERR_CUDA: return "W4_ERR_CUDA";
+    }
+    return "W4_ERR_UNKNOWN";
+}
+
+int w4_version(void) { return 10000; }
+
+w4_status w4_repacked_sizes(int K, int N, size_t *qweight_bytes, size_t *scales_bytes,
+                            size_t *zeros_bytes) {
+    if (!valid_kn(K, N) || !qweight_bytes || !scales_bytes || !zeros_bytes)
+        return W4_ERR_INVALID_ARG;
+    *qweight_bytes = w4::packed_qweight_bytes(K, N);
+    *scales_bytes = w4::packed_scales_bytes(K, N);
+    *zeros_bytes = w4::packed_zeros_bytes(K, N);
+    return W4_OK;
+}
+
+w4_status w4_repack(const uint32_t *qweight, const uint16_t *scales, const uint8_t *zeros, int K,
+                    int N, void *qweight_out, void *scales_out, void *zeros_out,
+                    w4_stream_t stream) {
+    if (!qweight || !scales || !zeros || !qweight_out || !scales_out || !zeros_out)
+        return W4_ERR_INVALID_ARG;
+    if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
+    if (!aligned(qweight, 4) || !aligned(scales, 2) || !aligned(qweight_out, 16) ||
+        !aligned(scales_out, 16))
+        return W4_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return W4_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return W4_ERR_UNSUPPORTED;
+    cudaError_t e = w4::launch_repack(qweight, scales, zeros, K, N, qweight_out, scales_out,
+                                      zeros_out, s);
+    if (e != cudaSuccess) return W4_ERR_CUDA;
+    w4::Header h;
+    e = cudaMemcpyAsync(&h, qweight_out, sizeof h, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return W4_ERR_CUDA;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return W4_ERR_CUDA;
+    return h.bad_zeros ? W4_ERR_INVALID_ARG : W4_OK;
+}
+
+w4_status w4_check_header(const void *header, int K, int N) {
+    if (!header) return W4_ERR_INVALID_ARG;
+    w4::Header h;
+    memcpy(&h, header, sizeof h);
+    if (memcmp(h.magic, "W4G128KL", 8) != 0 || h.layout_id != W4_LAYOUT_ID ||
+        h.version != W4_LAYOUT_VERSION || h.K != K || h.N != N || h.bad_zeros != 0)
+        return W4_ERR_LAYOUT;
+    return W4_OK;
+}
+
+w4_status w4_dequant(const uint32_t *qweight, const uint16_t *scales, const uint8_t *zeros, int K,
+                     int N, uint16_t *w_out, w4_stream_t stream) {
+    if (!qweight || !scales || !zeros || !w_out) return W4_ERR_INVALID_ARG;
+    if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
+    if (!aligned(qweight, 16) || !aligned(scales, 2) || !aligned(w_out, 16))
+        return W4_ERR_INVALID_ARG;
+    return cuda_status(w4::launch_dequant(qweight, scales, zeros, K, N, w_out,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4_status w4_gemv(const void *qweight, const void *scales, const void *zeros, const uint16_t *x,
+                  uint16_t *y, int M, int K, int N, w4_stream_t stream) {
+    return gemv_common(qweight, scales, zeros, x, y, false, M, K, N, stream);
+}
+
+w4_status w4_gemv_f32(const void *qweight, const void *scales, const void *zeros,
+                      const uint16_t *x, float *y, int M, int K, int N, w4_stream_t stream) {
+    return gemv_common(qweight, scales, zeros, x, y, true, M, K, N, stream);
+}
+
+w4_status w4_gemv_config(int K, int N, int *tiles_per_block, int *k_splits) {
+    if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return W4_ERR_CUDA;
+    w4::GemvShape shape;
+    if (!w4::gemv_shape(K, N, sms, &shape)) return W4_ERR_UNSUPPORTED;
+    if (tiles_per_block) *tiles_per_block = shape.warps;
+    if (k_splits) *k_splits = shape.splits;
+    return W4_OK;
+}
+
+}  // extern "C"

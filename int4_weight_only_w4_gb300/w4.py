@@ -1,0 +1,186 @@
+"""Thin ctypes binding to libw4.so (include/w4.h).  Argument marshalling only:
+every step of the computation runs in the library's CUDA kernels.
+
+Tensors are torch CUDA tensors (torch is used for device memory and streams).
+Each function enqueues on the given stream, or on torch's current stream of the
+tensor's device when ``stream`` is None, and raises W4Error on a non-OK status.
+Importing this module raises if the CUDA library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libw4.so")
+HEADER_BYTES = 128
+GROUP = 128
+MAX_TOKENS = 8
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build the CUDA library first "
+        "(python -c 'import __graft_entry__ as g; g.build()'). There is no CPU fallback.")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_ST = ctypes.c_int
+
+
+def _decl(name, res, *args):
+    fn = getattr(_lib, name)
+    fn.restype = res
+    fn.argtypes = list(args)
+    return fn
+
+
+_status_string = _decl("w4_status_string", ctypes.c_char_p, _ST)
+_version = _decl("w4_version", _I)
+_repacked_sizes = _decl("w4_repacked_sizes", _ST, _I, _I, ctypes.POINTER(ctypes.c_size_t),
+                        ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t))
+_repack = _decl("w4_repack", _ST, _P, _P, _P, _I, _I, _P, _P, _P, _P)
+_check_header = _decl("w4_check_header", _ST, _P, _I, _I)
+_dequant = _decl("w4_dequant", _ST, _P, _P, _P, _I, _I, _P, _P)
+_gemv = _decl("w4_gemv", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
+_gemv_f32 = _decl("w4_gemv_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
+_gemv_config = _decl("w4_gemv_config", _ST, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I))
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    INVALID_ARG = 1
+    UNSUPPORTED = 2
+    LAYOUT = 3
+    CUDA = 4
+
+
+class W4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = Status(status) if status in Status._value2member_map_ else status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def status_string(status: int) -> str:
+    return _status_string(int(status)).decode()
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def version() -> int:
+    return _version()
+
+
+def _ok(status: int, where: str) -> None:
+    if status != 0:
+        raise W4Error(status, where)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream, like: torch.Tensor):
+    if stream is None:
+        stream = torch.cuda.current_stream(like.device)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def repacked_sizes(K: int, N: int):
+    """Byte sizes (qweight, scales, zeros) of the kernel layout for N x K."""
+    q, s, z = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _ok(_repacked_sizes(K, N, ctypes.byref(q), ctypes.byref(s), ctypes.byref(z)),
+        "w4_repacked_sizes")
+    return q.value, s.value, z.value
+
+
+def repack(qweight, scales, zeros, K: int, N: int, qweight_out, scales_out, zeros_out,
+           stream=None) -> None:
+    """w4_repack: canonical device tensors -> the three kernel-layout buffers."""
+    _ok(_repack(_ptr(qweight), _ptr(scales), _ptr(zeros), K, N, _ptr(qweight_out),
+                _ptr(scales_out), _ptr(zeros_out), _stream(stream, qweight)), "w4_repack")
+
+
+def check_header(header_bytes: bytes, K: int, N: int) -> None:
+    buf = ctypes.create_string_buffer(bytes(header_bytes), HEADER_BYTES)
+    _ok(_check_header(ctypes.cast(buf, ctypes.c_void_p), K, N), "w4_check_header")
+
+
+def dequant(qweight, scales, zeros, K: int, N: int, w_out, stream=None) -> None:
+    """w4_dequant: canonical weights -> binary16 [N, K] (bit patterns in w_out)."""
+    _ok(_dequant(_ptr(qweight), _ptr(scales), _ptr(zeros), K, N, _ptr(w_out),
+                 _stream(stream, qweight)), "w4_dequant")
+
+
+def gemv(qweight, scales, zeros, x, y, M: int, K: int, N: int, stream=None) -> None:
+    """w4_gemv: y[M, N] (bfloat16) = W x with W in the kernel layout."""
+    _ok(_gemv(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, N,
+              _stream(stream, x)), "w4_gemv")
+
+
+def gemv_f32(qweight, scales, zeros, x, y, M: int, K: int, N: int, stream=None) -> None:
+    """w4_gemv_f32: as gemv but y is float32 (before the bfloat16 cast)."""
+    _ok(_gemv_f32(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, N,
+                  _stream(stream, x)), "w4_gemv_f32")
+
+
+def gemv_config(K: int, N: int):
+    """(16-row tiles per block, K splits) that w4_gemv uses for N x K."""
+    t, s = _I(), _I()
+    _ok(_gemv_config(K, N, ctypes.byref(t), ctypes.byref(s)), "w4_gemv_config")
+    return t.value, s.value
+
+
+@dataclass
+class PackedWeight:
+    """An N x K weight in the kernel layout (three device buffers)."""
+    K: int
+    N: int
+    qweight: torch.Tensor   # uint8 bytes, starts with the 128-byte header
+    scales: torch.Tensor    # uint8 bytes
+    zeros: torch.Tensor     # uint8 bytes
+
+    def gemv(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """y = W x for x bfloat16 [M, K] on the device; returns y bfloat16 [M, N]."""
+        M = x.shape[0]
+        if y is None:
+            y = torch.empty((M, self.N), dtype=torch.bfloat16, device=x.device)
+        gemv(self.qweight, self.scales, self.zeros, x, y, M, self.K, self.N, stream)
+        return y
+
+    def gemv_f32(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None):
+        M = x.shape[0]
+        if y is None:
+            y = torch.empty((M, self.N), dtype=torch.float32, device=x.device)
+        gemv_f32(self.qweight, self.scales, self.zeros, x, y, M, self.K, self.N, stream)
+        return y
+
+
+def pack(qweight: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor, K: int, N: int,
+         stream=None) -> PackedWeight:
+    """Allocate the kernel-layout buffers (torch), repack into them and check
+    the header once."""
+    dev = qweight.device
+    qb, sb, zb = repacked_sizes(K, N)
+    qo = torch.empty(qb, dtype=torch.uint8, device=dev)
+    so = torch.empty(sb, dtype=torch.uint8, device=dev)
+    zo = torch.empty(zb, dtype=torch.uint8, device=dev)
+    repack(qweight, scales, zeros, K, N, qo, so, zo, stream)
+    check_header(qo[:HEADER_BYTES].cpu().numpy().tobytes(), K, N)
+    return PackedWeight(K, N, qo, so, zo)

@@ -1,0 +1,245 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.  Dequantisation must be bit-exact; the GEMV must meet the
+tolerances in w4_testutil; closed-form cases must be exact."""
+import numpy as np
+import pytest
+
+import oracle
+from int4_weight_only_w4_gb300 import synthetic as syn
+from tests import w4_testutil as tu
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def w4():
+    from int4_weight_only_w4_gb300 import w4 as mod
+    return mod
+
+
+def run_gemv(w4, p, packed=None):
+    qw, sc, zp, x = tu.to_device(p)
+    if packed is None:
+        packed = w4.pack(qw, sc, zp, p.K, p.N)
+    y32 = packed.gemv_f32(x)
+    y16 = packed.gemv(x)
+    torch.cuda.synchronize()
+    return y32.cpu().numpy(), tu.bf16_bits(y16), packed
+
+
+def oracle_rows(p, rows):
+    return oracle.gemv_rows_f64(p.qweight, p.scales, p.zeros, p.x, p.M, p.K, p.N, rows,
+                                with_abs=True)
+
+
+def sample_rows(N, rng, count=1536):
+    if N <= count:
+        return np.arange(N)
+    head = np.arange(64)
+    tail = np.arange(N - 64, N)
+    mid = rng.choice(np.arange(64, N - 64), size=count - 128, replace=False)
+    return np.sort(np.concatenate([head, mid, tail]))
+
+
+# ---- dequantisation: bit-exact -------------------------------------------------
+
+@pytest.mark.parametrize("name", [s[0] for s in syn.SHAPES])
+def test_dequant_bit_exact(w4, name):
+    _, K, N, _, srange = syn.shape(name)
+    qwn, scn, zpn = syn.make_weights(name, K, N, seed=0, scale_range=srange)
+    p = syn.Problem(name, 1, K, N, qwn, scn, zpn, np.zeros((1, K), np.uint16))
+    qw, sc, zp, _ = tu.to_device(p)
+    out = torch.empty((N, K), dtype=torch.int16, device="cuda")
+    w4.dequant(qw, sc, zp, K, N, out)
+    got = out.cpu().numpy().view(np.uint16)
+    if N * K > 64 * 2 ** 20:      # compare a row sample on the largest weights
+        rows = sample_rows(N, np.random.default_rng(0), 2048)
+        want = oracle.dequant_f16(qwn[rows], scn[rows], zpn[rows], K, len(rows))
+        assert np.array_equal(got[rows], want)
+    else:
+        assert np.array_equal(got, oracle.dequant_f16(qwn, scn, zpn, K, N))
+
+
+def test_dequant_extreme_scales(w4):
+    rng = np.random.default_rng(3)
+    K, N = 256, 40
+    q = syn.uniform_words(1, "dq", (N, K // 8))
+    sc = rng.choice(np.array([0x0001, 0x03FF, 0x0400, 0x7BFF, 0x5A00, 0x3C01, 0x8001, 0xBC00],
+                             np.uint16), size=(N, 2))
+    zp = rng.integers(0, 16, size=(N, 2)).astype(np.uint8)
+    p = syn.Problem("dq", 1, K, N, q, sc, zp, np.zeros((1, K), np.uint16))
+    qw, scd, zpd, _ = tu.to_device(p)
+    out = torch.empty((N, K), dtype=torch.int16, device="cuda")
+    w4.dequant(qw, scd, zpd, K, N, out)
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), oracle.dequant_f16(q, sc, zp, K, N))
+
+
+# ---- GEMV at the workload shapes ------------------------------------------------
+
+CASES = [(name, M) for (name, K, N, Ms, _) in syn.SHAPES for M in Ms]
+
+
+@pytest.mark.parametrize("name,M", CASES)
+def test_gemv_workload_shapes(w4, name, M):
+    _, K, N, _, srange = syn.shape(name)
+    p = syn.make_problem(f"{name}.M{M}", K, N, M, seed=0, scale_range=srange)
+    got32, got16, _ = run_gemv(w4, p)
+    _, splits = w4.gemv_config(K, N)
+    rows = sample_rows(N, np.random.default_rng(1)) if M * N * K > 2 ** 28 else np.arange(N)
+    ref, refabs = oracle_rows(p, rows)
+    tu.check_gemv(got32[:, rows], got16[:, rows], ref, refabs, K, splits, f"{name} M={M}")
+
+
+# ---- edge cases ---------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K,N", [(1, 128, 1), (3, 128, 17), (8, 256, 200), (2, 1152, 1000),
+                                   (7, 384, 48), (4, 18944, 40), (5, 17408, 33),
+                                   (1, 640, 16), (6, 2048, 513)])
+def test_gemv_ragged_and_small(w4, M, K, N):
+    p = syn.make_problem(f"edge.{M}.{K}.{N}", K, N, M, seed=2)
+    got32, got16, _ = run_gemv(w4, p)
+    ref, refabs = oracle.gemv_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N, with_abs=True)
+    _, splits = w4.gemv_config(K, N)
+    tu.check_gemv(got32, got16, ref, refabs, K, splits, f"edge {M},{K},{N}")
+
+
+def test_split_paths_covered(w4):
+    splits = {w4.gemv_config(K, N)[1] for (_, K, N, _, _) in syn.SHAPES}
+    assert 1 in splits and any(s > 1 for s in splits), splits
+
+
+def test_q_equals_z_gives_exact_zero(w4):
+    M, K, N = 4, 1024, 100
+    p = syn.make_problem("qz", K, N, M, seed=4)
+    z = p.zeros
+    q = np.repeat(z, 128, axis=1).astype(np.uint32)
+    words = np.zeros((N, K // 8), np.uint32)
+    for j in range(8):
+        words |= q[:, j::8] << np.uint32(4 * j)
+    p.qweight = words
+    got32, got16, _ = run_gemv(w4, p)
+    assert np.all(got32 == 0.0) and np.all((got16 & 0x7FFF) == 0)
+
+
+def test_one_hot_and_identity_exact(w4):
+    M, K, N = 8, 512, 96
+    p = syn.make_problem("onehot", K, N, M, seed=5)
+    ks = [0, 1, 127, 128, 255, 300, 448, 511]
+    x = np.zeros((M, K), np.uint16)
+    vals = [0x3F80, 0xC040, 0x3E20, 0x4109, 0xBF00, 0x3F81, 0x4000, 0xC2F6]
+    for m in range(M):
+        x[m, ks[m]] = vals[m]
+    p.x = x
+    got32, _, _ = run_gemv(w4, p)
+    ref = oracle.gemv_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N)
+    assert np.array_equal(got32, ref.astype(np.float32))
+    # identity pattern: q - z = 1 on the diagonal, 0 elsewhere; y = s * x exactly
+    Kd = Nd = 256
+    z = np.random.default_rng(6).integers(0, 15, size=(Nd, Kd // 128))
+    q = np.repeat(z, 128, axis=1)
+    for n in range(Nd):
+        q[n, n] = z[n, n // 128] + 1
+    words = np.zeros((Nd, Kd // 8), np.uint32)
+    for j in range(8):
+        words |= q[:, j::8].astype(np.uint32) << np.uint32(4 * j)
+    pi = syn.make_problem("ident", Kd, Nd, 3, seed=7)
+    pi.qweight, pi.zeros = words, z.astype(np.uint8)
+    got32, _, _ = run_gemv(w4, pi)
+    ref = oracle.gemv_f64(pi.qweight, pi.scales, pi.zeros, pi.x, 3, Kd, Nd)
+    assert np.array_equal(got32, ref.astype(np.float32))
+
+
+def test_linearity_power_of_two_exact(w4):
+    M, K, N = 3, 3584, 300
+    p = syn.make_problem("lin", K, N, M, seed=8)
+    a32, _, packed = run_gemv(w4, p)
+    xf = (p.x.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0)
+    p2 = syn.Problem("lin2", M, K, N, p.qweight, p.scales, p.zeros,
+                     (xf.view(np.uint32) >> 16).astype(np.uint16))
+    b32, _, _ = run_gemv(w4, p2, packed)
+    assert np.array_equal(b32, 2 * a32)
+
+
+def test_determinism_and_batch_invariance(w4):
+    K, N = 18944, 3584
+    p = syn.make_problem("det", K, N, 8, seed=9)
+    qw, sc, zp, x = tu.to_device(p)
+    packed = w4.pack(qw, sc, zp, K, N)
+    first = packed.gemv_f32(x).cpu()
+    for _ in range(50):
+        assert torch.equal(packed.gemv_f32(x).cpu(), first)
+    for r in (0, 3, 7):
+        one = packed.gemv_f32(x[r:r + 1].contiguous()).cpu()
+        assert torch.equal(one[0], first[r])
+    five = packed.gemv_f32(x[:5].contiguous()).cpu()
+    assert torch.equal(five, first[:5])
+
+
+def test_graph_capture_replay(w4):
+    K, N, M = 3584, 4608, 1
+    p = syn.make_problem("graph", K, N, M, seed=10)
+    qw, sc, zp, x = tu.to_device(p)
+    packed = w4.pack(qw, sc, zp, K, N)
+    y_eager = packed.gemv(x)
+    y = torch.empty_like(y_eager)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        packed.gemv(x, y)            # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        packed.gemv(x, y)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_eager)
+
+
+def test_repack_rejects_bad_zero_and_capture(w4):
+    K, N = 256, 32
+    p = syn.make_problem("badz", K, N, 1, seed=11)
+    p.zeros[5, 1] = 16
+    qw, sc, zp, _ = tu.to_device(p)
+    with pytest.raises(w4.W4Error) as e:
+        w4.pack(qw, sc, zp, K, N)
+    assert e.value.status == w4.Status.INVALID_ARG
+    # a stream being captured: repack synchronises, so it refuses
+    p.zeros[5, 1] = 3
+    qw, sc, zp, _ = tu.to_device(p)
+    qb, sb, zb = w4.repacked_sizes(K, N)
+    bufs = [torch.empty(n, dtype=torch.uint8, device="cuda") for n in (qb, sb, zb)]
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            with pytest.raises(w4.W4Error) as e2:
+                w4.repack(qw, sc, zp, K, N, *bufs, stream=s)
+    assert e2.value.status == w4.Status.UNSUPPORTED
+
+
+def test_header_checked(w4):
+    K, N = 384, 64
+    p = syn.make_problem("hdr", K, N, 1, seed=12)
+    qw, sc, zp, _ = tu.to_device(p)
+    packed = w4.pack(qw, sc, zp, K, N)
+    hdr = packed.qweight[:128].cpu().numpy().tobytes()
+    w4.check_header(hdr, K, N)
+    with pytest.raises(w4.W4Error):
+        w4.check_header(hdr, K, N + 16)
+
+
+def test_argument_errors_on_device(w4):
+    K, N = 256, 32
+    p = syn.make_problem("args", K, N, 2, seed=13)
+    qw, sc, zp, x = tu.to_device(p)
+    packed = w4.pack(qw, sc, zp, K, N)
+    y = torch.empty((2, N), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(w4.W4Error) as e:
+        w4.gemv(packed.qweight, packed.scales, packed.zeros, x, y, 9, K, N)
+    assert e.value.status == w4.Status.UNSUPPORTED
+    with pytest.raises(w4.W4Error) as e:
+        w4.gemv(packed.qweight, packed.scales, packed.zeros, x, y, 2, 200, N)
+    assert e.value.status == w4.Status.INVALID_ARG

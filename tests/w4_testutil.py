@@ -1,0 +1,71 @@
+"""Helpers shared by the GPU parity tests: device upload and the comparison
+rules.  The rules follow the library's stated tolerances:
+  * relative L2 error of the fp32 output (before the bfloat16 cast) <= 1e-3,
+  * max |error| <= 1e-2 * max |y_ref|,
+  * bfloat16 output within 1 ulp of round-to-nearest-even(y_ref) -- except
+    where a bfloat16 ulp at y_ref is smaller than the fp32 rounding-error bound
+    of the sum itself (tiny |y_ref| from cancellation), in which case the fp32
+    output must lie within that bound.
+The bound is the textbook one for a sum evaluated with n sequential roundings,
+|error| <= n * u * sum_k |w_k x_k|, with u = 2^-23 (one fp32 ulp, which also
+covers truncating accumulation) and n = 8 k-steps per group + G groups + the
+number of K splits + 1.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+REL_L2 = 1e-3
+MAX_ABS_FRAC = 1e-2
+
+
+def to_device(p, dev="cuda"):
+    import torch
+    qw = torch.from_numpy(np.ascontiguousarray(p.qweight).view(np.int32)).to(dev)
+    sc = torch.from_numpy(np.ascontiguousarray(p.scales).view(np.int16)).to(dev)
+    zp = torch.from_numpy(np.ascontiguousarray(p.zeros)).to(dev)
+    x = torch.from_numpy(np.ascontiguousarray(p.x).view(np.int16)).to(dev).view(torch.bfloat16)
+    return qw, sc, zp, x
+
+
+def x_to_device(xbits, dev="cuda"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(xbits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def bf16_bits(t) -> np.ndarray:
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def ordered(bits: np.ndarray) -> np.ndarray:
+    """Map bfloat16 bit patterns to integers whose difference counts ulps."""
+    b = bits.astype(np.int64)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b)
+
+
+def check_gemv(got32: np.ndarray, got16: np.ndarray, ref64: np.ndarray, refabs: np.ndarray,
+               K: int, splits: int, what: str = "") -> dict:
+    ref32 = ref64.astype(np.float32)
+    err = got32.astype(np.float64) - ref64
+    nref = np.linalg.norm(ref32.astype(np.float64))
+    rel = np.linalg.norm(err) / nref if nref > 0 else np.linalg.norm(err)
+    maxabs = np.abs(err).max() if err.size else 0.0
+    maxref = np.abs(ref32).max() if ref32.size else 0.0
+    assert rel <= REL_L2, f"{what}: relative L2 error {rel:.3e} > {REL_L2}"
+    assert maxabs <= MAX_ABS_FRAC * maxref + 0.0, f"{what}: max abs error {maxabs:.3e}"
+    want16 = oracle.bf16_rne(ref32)
+    ulps = np.abs(ordered(got16) - ordered(want16))
+    off = ulps > 1
+    n_steps = 8 + K // 128 + splits + 1
+    bound = n_steps * 2.0 ** -23 * refabs
+    if off.any():
+        worst = np.abs(err[off]) - bound[off]
+        assert (worst <= 0).all(), (
+            f"{what}: {int(off.sum())} bf16 outputs off by >1 ulp beyond the fp32 bound "
+            f"(worst excess {worst.max():.3e})")
+    # the bfloat16 output is the nearest-even rounding of the fp32 output
+    assert np.array_equal(got16, oracle.bf16_rne(got32)), f"{what}: bf16 != rne(fp32)"
+    return {"rel_l2": float(rel), "max_abs": float(maxabs), "ulp_gt1": int(off.sum())}
