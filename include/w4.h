@@ -58,7 +58,7 @@ typedef enum w4_status {
 #define W4_GROUP_SIZE 128
 #define W4_MAX_TOKENS 8
 #define W4_LAYOUT_ID 1
-#define W4_LAYOUT_VERSION 1
+#define W4_LAYOUT_VERSION 2
 #define W4_HEADER_BYTES 128
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -69,9 +69,11 @@ int w4_version(void);
 
 /*
  * Sizes in bytes of the three buffers that w4_repack writes for an N x K
- * weight (the kernel layout).  The qweight buffer starts with a
- * W4_HEADER_BYTES header (layout id, version, K, N).  Rows are padded to a
- * multiple of 16 inside the buffers; the padding is never read back as output.
+ * weight (the kernel layout): with NB = ceil(N / 128) row blocks and
+ * G = K / 128 groups, qweight = W4_HEADER_BYTES + NB*G*8192, scales =
+ * NB*G*256, zeros = NB*G*64.  The qweight buffer starts with a header
+ * (layout id, version, K, N, error words).  Rows are padded to a multiple of
+ * 128 with zero weights; the padding is never written back as output.
  * Errors: W4_ERR_INVALID_ARG for bad K/N or a NULL output pointer.
  */
 w4_status w4_repacked_sizes(int K, int N, size_t *qweight_bytes,
@@ -85,8 +87,8 @@ w4_status w4_repacked_sizes(int K, int N, size_t *qweight_bytes,
  *
  *   qweight, scales, zeros : device, canonical layout (see top); qweight 16-byte
  *                            aligned, scales 2-byte aligned
- *   qweight_out, scales_out, zeros_out : device, sizes from w4_repacked_sizes;
- *                            qweight_out and scales_out 16-byte aligned
+ *   qweight_out, scales_out, zeros_out : device, sizes from w4_repacked_sizes,
+ *                            each 16-byte aligned
  *
  * Validates every zero point on the device (must be <= 15) and therefore
  * synchronises `stream` before returning: not capturable into a CUDA graph
@@ -102,7 +104,8 @@ w4_status w4_repack(const uint32_t *qweight, const uint16_t *scales,
  * Host-side check of a repacked qweight buffer's header.  `header` is a host
  * copy of its first W4_HEADER_BYTES bytes.  Returns W4_OK when the magic,
  * layout id and version are this library's and K, N match; W4_ERR_LAYOUT
- * otherwise; W4_ERR_INVALID_ARG for a NULL pointer.
+ * otherwise; W4_ERR_CUDA if a w4_gemv on this weight recorded that it gave up
+ * waiting for its own copies (see w4_gemv); W4_ERR_INVALID_ARG for NULL.
  */
 w4_status w4_check_header(const void *header, int K, int N);
 
@@ -130,12 +133,16 @@ w4_status w4_dequant(const uint32_t *qweight, const uint16_t *scales,
  * and "qengine", section "How it works" (4-bit matrix-vector kernel, partial
  * sums added in a fixed order).
  *
- *   qweight, scales, zeros : device, the three buffers of w4_repack; qweight
- *                            16-byte aligned, scales 4-byte aligned
- *   x                      : device, bfloat16 [M][K], 4-byte aligned
+ *   qweight, scales, zeros : device, the three buffers of w4_repack, each
+ *                            16-byte aligned
+ *   x                      : device, bfloat16 [M][K], 16-byte aligned
  *   y                      : device, bfloat16 [M][N], 2-byte aligned
  * The header is not read here (that would need a device read); check it once
- * with w4_check_header.
+ * with w4_check_header.  Every wait inside the kernel is bounded: a block that
+ * gives up (about 2 s without progress -- never in normal operation) sets the
+ * header's error word, which w4_check_header then reports, and leaves its
+ * outputs unwritten.  Weights, scales and zeros must not be written by work
+ * still running on the device when w4_gemv is enqueued.
  * Errors: W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED (M outside 1..8), W4_ERR_CUDA.
  */
 w4_status w4_gemv(const void *qweight, const void *scales, const void *zeros,

@@ -30,8 +30,8 @@ w4_status gemv_common(const void *qweight, const void *scales, const void *zeros
     if (!qweight || !scales || !zeros || !x || !y) return W4_ERR_INVALID_ARG;
     if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
     if (M < 1 || M > W4_MAX_TOKENS) return W4_ERR_UNSUPPORTED;
-    if (!aligned(qweight, 16) || !aligned(scales, 4) || !aligned(x, 4) ||
-        !aligned(y, f32_out ? 4 : 2))
+    if (!aligned(qweight, 16) || !aligned(scales, 16) || !aligned(zeros, 16) ||
+        !aligned(x, 16) || !aligned(y, f32_out ? 4 : 2))
         return W4_ERR_INVALID_ARG;
     const int sms = device_sms();
     if (sms <= 0) return W4_ERR_CUDA;
@@ -75,7 +75,7 @@ w4_status w4_repack(const uint32_t *qweight, const uint16_t *scales, const uint8
         return W4_ERR_INVALID_ARG;
     if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
     if (!aligned(qweight, 4) || !aligned(scales, 2) || !aligned(qweight_out, 16) ||
-        !aligned(scales_out, 16))
+        !aligned(scales_out, 16) || !aligned(zeros_out, 16))
         return W4_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -99,6 +99,7 @@ w4_status w4_check_header(const void *header, int K, int N) {
     if (memcmp(h.magic, "W4G128KL", 8) != 0 || h.layout_id != W4_LAYOUT_ID ||
         h.version != W4_LAYOUT_VERSION || h.K != K || h.N != N || h.bad_zeros != 0)
         return W4_ERR_LAYOUT;
+    if (h.kernel_error != 0) return W4_ERR_CUDA;
     return W4_OK;
 }
 

@@ -1,32 +1,42 @@
 // w4_gemv: fused INT4-dequantise + matrix-vector product for sm_103a.
 //
-// Work split.  A thread block of `warps` warps owns `warps` consecutive
-// 16-row tiles (one per warp) and one slice of K.  With `splits` > 1 the
-// K slices of the same tiles are handled by the `splits` blocks of one thread
-// block cluster, which combine their fp32 partial sums through distributed
-// shared memory in a fixed rank order: deterministic, no workspace, no float
-// atomics ("qengine", section "Learnings": float atomics made one run in fifty
-// differ; a fixed summation order fixed it).
+// Work split.  One thread block owns one row block (8 tiles of 16 rows, see
+// w4_repack.cu) and one slice of K.  With `splits` > 1 the K slices of a row
+// block are handled by the `splits` blocks of one thread-block cluster, which
+// combine their fp32 partial sums through distributed shared memory in a fixed
+// rank order: deterministic, no workspace, no float atomics ("qengine",
+// section "Learnings": float atomics made one run in fifty differ; a fixed
+// summation order fixed it).
 //
-// Per warp.  Each lane streams its 16-byte pieces of the packed weights (see
-// w4_repack.cu for the layout) with L1-bypassing 128-bit loads, keeping kInFlight
-// pieces in flight.  A piece holds 64 k of its fragment rows; each of its four
-// words is turned into the four bf16x2 registers of a tensor-core A fragment
-// without any conversion instruction: (word >> 4p) & 0x000F000F | 0x43004300
-// is the bf16 pair (128 + q_even, 128 + q_odd) exactly (bf16 has 7 fraction
-// bits, so 128 + q for q < 128 is exact), and one bf16x2 subtraction of
-// (128 + z) leaves q - z exactly.  mma.m16n8k16 (bf16 inputs, fp32
-// accumulation) then multiplies the 16 x 16 weight block with up to 8 token
-// columns of x.  The products q - z times x are exact; the scale is applied
-// once per group of 128 in fp32: acc += s * sum_group (q - z) x.
+// Streaming.  A producer warp moves the block's weights group by group
+// (one 8 KB weight record + 256 B of scales + 64 B of zeros per group) into a
+// ring of shared-memory stages with bulk asynchronous copies (cp.async.bulk,
+// completion counted in bytes on an mbarrier), and the block's K slice of x
+// once at the start.  Eight consumer warps (one per 16-row tile) wait on a
+// stage's "full" barrier, copy their part of it into registers and release it
+// on the stage's "empty" barrier, so the producer keeps `stages` groups (up
+// to ~50 KB per block) in flight: the copy engine, not per-thread loads,
+// carries the bytes in flight that HBM needs.  This is the one-producer,
+// several-consumers, transaction-counted-barrier arrangement of "Building an
+// LLM Inference Runtime ...", section "Bug #1", applied to weight streaming.
 //
-// x staging.  Each block copies its K slice of x (bf16 pairs, no arithmetic)
-// to shared memory, permuted so that each lane's eight B-fragment registers
-// for one 64-k piece are two consecutive 16-byte words.  Lanes whose token
-// column is >= M feed zeros.  The shape (warps, splits) depends only on K and N,
-// so the result for one token does not depend on M (batch invariance,
-// "qengine", section "How it works": identical results for row r whether 1 or
-// 8 rows are processed).
+// Per consumer warp and group.  The 16-byte piece a lane owns in each 64-k
+// chunk holds four k-steps of its tensor-core A fragment.  Each word becomes
+// the four bf16x2 A registers without a conversion instruction:
+// (word >> 4p) & 0x000F000F | 0x43004300 is the bf16 pair (128 + q_even,
+// 128 + q_odd) exactly (bf16 has 7 fraction bits, so 128 + q is exact for
+// q < 128), and one bf16x2 fma adding -(128 + z) leaves q - z exactly.
+// mma.m16n8k16 (bf16 inputs, fp32 accumulation) multiplies the 16 x 16
+// weight block with up to 8 token columns of x; the products (q - z) * x are
+// exact, and the group scale is applied once per group in fp32:
+// acc += s * sum_group (q - z) x.  Lanes whose token column is >= M feed
+// zeros.  The launch shape depends only on K and N, so the result for one
+// token does not depend on M or on the other tokens (batch invariance,
+// "qengine", section "How it works").
+//
+// Waits are bounded: a wait that exceeds ~2 s of clock cycles gives up, the
+// block records the failure in the header's kernel_error word and skips the
+// rest of its work; it never spins forever.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -38,35 +48,81 @@ namespace cg = cooperative_groups;
 namespace w4 {
 namespace {
 
-constexpr int kInFlight = 8;      // 16-byte pieces per lane in flight (even)
-constexpr int kWarps = 8;         // warps (16-row tiles) per block
-constexpr size_t kMaxXBytes = 200 * 1024;   // shared-memory budget for staged x
+constexpr int kWarps = kBlockTiles;                 // consumer warps
+constexpr int kThreads = (kWarps + 1) * 32;         // + one producer warp
+constexpr int kStageBytes = kRecWeights + kRecScales + kRecZeros;   // 8512
+constexpr int kMinStages = 4;                       // ring depth the split choice assumes
+constexpr int kMaxStages = 12;                      // deepest ring a launch uses
+constexpr size_t kBlockSmemBudget = 113 * 1024;     // two blocks per SM
+constexpr long long kWaitLimit = 4000000000LL;      // clock cycles (~2 s)
+constexpr size_t kOverlapBelowBytes = 16u << 20;    // packed weights of a "short" product
 
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
+// ---- PTX wrappers ---------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint32_t ld_nc_u32(const uint32_t *p) {
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete; false if the wait gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitLimit) return false;
+    }
+    return true;
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue now / wait until the previous kernel in the stream has completed
+// and its writes are visible.
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// a * 1 + c on a bf16 pair; with c = -(128 + z) this is (128 + q) - (128 + z)
+// = q - z, exact.
+__device__ __forceinline__ uint32_t bf16x2_add(uint32_t a, uint32_t c) {
     uint32_t r;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(0x3F803F80u), "r"(c));
     return r;
-}
-
-__device__ __forceinline__ uint32_t ld_nc_u8(const uint8_t *p) {
-    uint16_t r;
-    asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(r) : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
-    __nv_bfloat162 va = *reinterpret_cast<__nv_bfloat162 *>(&a);
-    __nv_bfloat162 vb = *reinterpret_cast<__nv_bfloat162 *>(&b);
-    __nv_bfloat162 r = __hsub2(va, vb);
-    return *reinterpret_cast<uint32_t *>(&r);
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -79,22 +135,57 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One 16-byte piece: four k-steps of 16.
-__device__ __forceinline__ void piece_mma(float (&d)[4], const uint4 &w, const uint32_t (&b)[8],
-                                          uint32_t czl, uint32_t czh) {
+// d = A * B (accumulator starts from the zero registers zq).
+__device__ __forceinline__ void mma_bf16_16816_first(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                     uint32_t a2, uint32_t a3, uint32_t b0,
+                                                     uint32_t b1, const float (&zq)[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(zq[0]), "f"(zq[1]),
+          "f"(zq[2]), "f"(zq[3]));
+}
+
+// (w & mask) | magic in one three-input logic operation.
+__device__ __forceinline__ uint32_t and_or(uint32_t w, uint32_t mask, uint32_t magic) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(mask), "r"(magic));
+    return r;
+}
+
+// Barrier over the eight consumer warps only (the producer warp is busy).
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"r"(kWarps * 32) : "memory");
+}
+
+// One 64-k chunk: four k-steps j; steps 0, 1 go to accumulator d[0] and steps
+// 2, 3 to d[1] (two independent chains).  bl, bh hold this lane's eight B
+// registers for the chunk (pairs (k, k+1) and (k+8, k+9) of each step).
+// ncl, nch = -(128 + z) for rows gq and gq + 8 as bf16 pairs.  mask and magic
+// are 0x000F000F and 0x43004300, passed in registers so that each extraction
+// is one three-input logic operation.  FIRST: the accumulators start from zero.
+template <bool FIRST>
+__device__ __forceinline__ void chunk_mma(float (&d)[2][4], const uint4 &w, const uint4 &bl,
+                                          const uint4 &bh, uint32_t ncl, uint32_t nch,
+                                          const float (&zq)[4], uint32_t mask, uint32_t magic) {
     const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+    const uint32_t b[8] = {bl.x, bl.y, bl.z, bl.w, bh.x, bh.y, bh.z, bh.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const uint32_t wd = words[j];
-        uint32_t a0 = (wd & 0x000F000Fu) | 0x43004300u;
-        uint32_t a1 = ((wd >> 4) & 0x000F000Fu) | 0x43004300u;
-        uint32_t a2 = ((wd >> 8) & 0x000F000Fu) | 0x43004300u;
-        uint32_t a3 = ((wd >> 12) & 0x000F000Fu) | 0x43004300u;
-        a0 = bf16x2_sub(a0, czl);
-        a1 = bf16x2_sub(a1, czh);
-        a2 = bf16x2_sub(a2, czl);
-        a3 = bf16x2_sub(a3, czh);
-        mma_bf16_16816(d, a0, a1, a2, a3, b[2 * j], b[2 * j + 1]);
+        uint32_t a0 = and_or(wd, mask, magic);
+        uint32_t a1 = and_or(wd >> 4, mask, magic);
+        uint32_t a2 = and_or(wd >> 8, mask, magic);
+        uint32_t a3 = and_or(wd >> 12, mask, magic);
+        a0 = bf16x2_add(a0, ncl);
+        a1 = bf16x2_add(a1, nch);
+        a2 = bf16x2_add(a2, ncl);
+        a3 = bf16x2_add(a3, nch);
+        if (FIRST && (j & 1) == 0)
+            mma_bf16_16816_first(d[j >> 1], a0, a1, a2, a3, b[2 * j], b[2 * j + 1], zq);
+        else
+            mma_bf16_16816(d[j >> 1], a0, a1, a2, a3, b[2 * j], b[2 * j + 1]);
     }
 }
 
@@ -104,7 +195,6 @@ __device__ __forceinline__ void store_tile(void *yv, const float (&acc)[4], int 
     const int gq = lane >> 2, tq = lane & 3;
     const int r0 = t * kTileRows + gq, r1 = r0 + 8;
     const int m0 = 2 * tq, m1 = m0 + 1;
-    const float v[4] = {acc[0], acc[1], acc[2], acc[3]};
     const int ms[4] = {m0, m1, m0, m1};
     const int rs[4] = {r0, r0, r1, r1};
 #pragma unroll
@@ -112,132 +202,198 @@ __device__ __forceinline__ void store_tile(void *yv, const float (&acc)[4], int 
         if (ms[i] < M && rs[i] < N) {
             const size_t o = (size_t)ms[i] * N + rs[i];
             if (F32OUT)
-                static_cast<float *>(yv)[o] = v[i];
+                static_cast<float *>(yv)[o] = acc[i];
             else
-                static_cast<__nv_bfloat16 *>(yv)[o] = __float2bfloat16_rn(v[i]);
+                static_cast<__nv_bfloat16 *>(yv)[o] = __float2bfloat16_rn(acc[i]);
         }
     }
 }
 
-template <bool F32OUT>
-__global__ void __launch_bounds__(kWarps * 32)
-gemv_kernel(const uint4 *__restrict__ qw, const uint32_t *__restrict__ sc,
-            const uint8_t *__restrict__ zp, const uint32_t *__restrict__ x32,
-            void *__restrict__ yv, int M, int K, int N, int T, int S) {
-    extern __shared__ __align__(16) uint32_t smem[];
+struct SmemPlan {
+    size_t x_off, x_row_bytes, zero_off, red_off, bar_off, total;
+};
+
+// Shared memory: [stages][weights | scales | zeros] [x rows, permuted in place
+// into B-fragment order] [256 zero bytes] [partials] [barriers]
+__host__ __device__ inline SmemPlan smem_plan(int K, int S, int M, int stages) {
     const int G = K / kGroup;
-    const int C = K / kChunkK;
+    const int gmax = (G + S - 1) / S;
+    SmemPlan p;
+    p.x_off = (size_t)stages * kStageBytes;
+    p.x_row_bytes = (size_t)gmax * kGroup * 2 + 16;      // +16 B: rows land on other banks
+    p.zero_off = p.x_off + (size_t)M * p.x_row_bytes;
+    p.red_off = p.zero_off + 256;
+    p.bar_off = p.red_off + (S > 1 ? (size_t)kWarps * 32 * 16 : 0);
+    p.total = p.bar_off + (size_t)(2 * kMaxStages + 1) * 8;
+    return p;
+}
+
+template <bool F32OUT>
+__global__ void __launch_bounds__(kThreads, 2)
+gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
+            const char *__restrict__ zp, const __nv_bfloat16 *__restrict__ x,
+            void *__restrict__ yv, uint32_t *err, int M, int K, int N, int S, int stages,
+            uint32_t nib_mask, uint32_t bf16_magic) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int G = K / kGroup;
+    const int b = blockIdx.x;
     const int split = blockIdx.y;
     const int g0 = (int)((long long)split * G / S);
     const int g1 = (int)((long long)(split + 1) * G / S);
-    const int c0 = 2 * g0;
-    const int nch = 2 * (g1 - g0);
+    const int ng = g1 - g0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gq = lane >> 2, tq = lane & 3;
-    const int t = blockIdx.x * kWarps + warp;
-    const bool active = t < T;
+    const SmemPlan plan = smem_plan(K, S, M, stages);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + plan.bar_off);
+    uint64_t *empty = full + kMaxStages;
+    uint64_t *xbar = empty + kMaxStages;
+    unsigned char *xs = smem + plan.x_off;
 
-    // Issue the first weight and group-metadata loads before staging x.
-    const uint4 *wp = qw + ((size_t)t * C + c0) * 32 + lane;
-    const size_t meta0 = ((size_t)t * G + g0) * 8 + gq;
-    uint4 ring[kInFlight];
-    uint32_t sring[kInFlight / 2], zring[kInFlight / 2];
-#pragma unroll
-    for (int i = 0; i < kInFlight / 2; ++i) sring[i] = zring[i] = 0u;
-#pragma unroll
-    for (int i = 0; i < kInFlight; ++i) {
-        ring[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (active && i < nch) {
-            ring[i] = ld_stream(wp + (size_t)i * 32);
-            if ((i & 1) == 0) {
-                sring[i / 2] = ld_nc_u32(sc + meta0 + (size_t)(i / 2) * 8);
-                zring[i / 2] = ld_nc_u8(zp + meta0 + (size_t)(i / 2) * 8);
-            }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
         }
-    }
-
-    // Stage this block's K slice of x: xs[(piece * M + m) * 4 + tq][8 words].
-    uint32_t *xs = smem;
-    {
-        const int per_row = nch * 32;            // bf16 pairs of one token in the slice
-        const size_t row_words = (size_t)K / 2;
-        for (int i = threadIdx.x; i < M * per_row; i += kWarps * 32) {
-            const int m = i / per_row, r = i - m * per_row;
-            const int cl = r >> 5, u = r & 31;
-            const int j = u >> 3, o = u & 7;
-            const uint32_t v = x32[(size_t)m * row_words + (size_t)(c0 + cl) * 32 + u];
-            xs[((cl * M + m) * 4 + (o & 3)) * 8 + 2 * j + (o >> 2)] = v;
-        }
+        mbar_init(xbar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
+    bool ok = true;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (active) {
-        const uint32_t *xl = xs + (gq * 4 + tq) * 8;
-        const bool has_x = gq < M;
-        const int piece_stride = M * 32;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t czl = 0u, czh = 0u;
-        float sl = 0.f, sh = 0.f;
-        for (int base = 0; base < nch; base += kInFlight) {
-#pragma unroll
-            for (int i = 0; i < kInFlight; ++i) {
-                const int ci = base + i;
-                if (ci < nch) {
-                    const uint4 w = ring[i];
-                    if ((i & 1) == 0) {
-                        const uint32_t zb = zring[i / 2], sp = sring[i / 2];
-                        czl = ((zb & 0xFu) | 0x4300u) * 0x10001u;
-                        czh = (((zb >> 4) & 0xFu) | 0x4300u) * 0x10001u;
-                        sl = __half2float(__ushort_as_half((unsigned short)(sp & 0xFFFFu)));
-                        sh = __half2float(__ushort_as_half((unsigned short)(sp >> 16)));
-                        d[0] = d[1] = d[2] = d[3] = 0.f;
-                    }
-                    const int nx = ci + kInFlight;
-                    if (nx < nch) {
-                        ring[i] = ld_stream(wp + (size_t)nx * 32);
-                        if ((i & 1) == 0) {
-                            sring[i / 2] = ld_nc_u32(sc + meta0 + (size_t)(nx / 2) * 8);
-                            zring[i / 2] = ld_nc_u8(zp + meta0 + (size_t)(nx / 2) * 8);
-                        }
-                    }
-                    uint32_t b[8];
-                    if (has_x) {
-                        const uint4 *bp = reinterpret_cast<const uint4 *>(xl + ci * piece_stride);
-                        const uint4 b0 = bp[0], b1 = bp[1];
-                        b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
-                        b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) b[q] = 0u;
-                    }
-                    piece_mma(d, w, b, czl, czh);
-                    if (i & 1) {
-                        acc[0] = fmaf(d[0], sl, acc[0]);
-                        acc[1] = fmaf(d[1], sl, acc[1]);
-                        acc[2] = fmaf(d[2], sh, acc[2]);
-                        acc[3] = fmaf(d[3], sh, acc[3]);
-                    }
+    // A following launch that opted into programmatic dependent launch may
+    // start its prologue (and its own weight copies) from here on.
+    allow_dependents();
+    if (warp == kWarps) {
+        // ---- producer ----
+        if (lane == 0) {
+            // The weights do not depend on the previous kernel in the stream:
+            // request the first two groups before waiting for it, then x (which
+            // the consumers need first), then the rest.
+            int issued = 0, slot = 0;
+            uint32_t phase = 0;                     // completed uses of `slot`, mod 2
+            const int first = ng < 2 ? ng : 2;
+            for (int s = 0; s < ng; ++s) {
+                if (s == first) {
+                    wait_prerequisites();
+                    mbar_expect_tx(xbar, (uint32_t)(M * ng * kGroup * 2));
+                    for (int m = 0; m < M; ++m)
+                        bulk_g2s(xs + m * plan.x_row_bytes,
+                                 x + (size_t)m * K + (size_t)g0 * kGroup,
+                                 (uint32_t)(ng * kGroup * 2), xbar);
+                }
+                if (s >= stages && !mbar_wait(&empty[slot], phase ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char *st = smem + (size_t)slot * kStageBytes;
+                const size_t rec = (size_t)b * G + g0 + s;
+                mbar_expect_tx(&full[slot], kStageBytes);
+                bulk_g2s(st, qw + W4_HEADER_BYTES + rec * kRecWeights, kRecWeights, &full[slot]);
+                bulk_g2s(st + kRecWeights, sc + rec * kRecScales, kRecScales, &full[slot]);
+                bulk_g2s(st + kRecWeights + kRecScales, zp + rec * kRecZeros, kRecZeros,
+                         &full[slot]);
+                ++issued;
+                if (++slot == stages) {
+                    slot = 0;
+                    phase ^= 1u;
                 }
             }
+            if (ng == first) {
+                wait_prerequisites();
+                mbar_expect_tx(xbar, (uint32_t)(M * ng * kGroup * 2));
+                for (int m = 0; m < M; ++m)
+                    bulk_g2s(xs + m * plan.x_row_bytes, x + (size_t)m * K + (size_t)g0 * kGroup,
+                             (uint32_t)(ng * kGroup * 2), xbar);
+            }
+            if (!ok) {
+                // Give the copies already issued a bounded chance to land before exit.
+                for (int s = issued > stages ? issued - stages : 0; s < issued; ++s)
+                    mbar_wait(&full[s % stages], (s / stages) & 1);
+                atomicOr(err, 1u);
+            }
         }
+    } else {
+        // ---- consumers: warp w owns tile 8b + w ----
+        const int gq = lane >> 2, tq = lane & 3;
+        // Token columns >= M read a 256-byte zero patch at a fixed address.
+        uint32_t *zpatch = reinterpret_cast<uint32_t *>(smem + plan.zero_off);
+        if (threadIdx.x < 64) zpatch[threadIdx.x] = 0u;
+        // Wait for x, then permute each 64-k segment of each token row in place
+        // (one warp per segment): word u of the segment (k = 64c + 2u, step
+        // j = u / 8, o = u % 8) moves to (o % 4) * 8 + 2j + o / 4, so that lane tq
+        // finds its eight B registers for the chunk as two 16-byte words.
+        if (!mbar_wait(xbar, 0)) ok = false;
+        for (int seg = warp; seg < M * ng * 2; seg += kWarps) {
+            const int m = seg / (ng * 2), c = seg - m * (ng * 2);
+            uint32_t *row = reinterpret_cast<uint32_t *>(xs + (size_t)m * plan.x_row_bytes) + c * 32;
+            const uint32_t v = row[lane];
+            __syncwarp();
+            row[(lane & 3) * 8 + 2 * (lane >> 3) + ((lane >> 2) & 1)] = v;
+        }
+        consumer_sync();
+        const bool has_x = gq < M;
+        const uint32_t *xrow =
+            (has_x ? reinterpret_cast<const uint32_t *>(xs + (size_t)gq * plan.x_row_bytes)
+                   : zpatch) + tq * 8;
+        const int xstride = has_x ? 64 : 0;     // words per group
+        const float zq[4] = {0.f, 0.f, 0.f, 0.f};
+        int slot = 0;
+        uint32_t phase = 0;
+        for (int s = 0; s < ng && ok; ++s) {
+            if (!mbar_wait(&full[slot], phase)) {
+                ok = false;
+                break;
+            }
+            const unsigned char *st = smem + (size_t)slot * kStageBytes;
+            const uint4 w0 = *reinterpret_cast<const uint4 *>(st + warp * 1024 + lane * 16);
+            const uint4 w1 = *reinterpret_cast<const uint4 *>(st + warp * 1024 + 512 + lane * 16);
+            const uint32_t sp =
+                *reinterpret_cast<const uint32_t *>(st + kRecWeights + warp * 32 + gq * 4);
+            const uint32_t zb = st[kRecWeights + kRecScales + warp * 8 + gq];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (++slot == stages) {
+                slot = 0;
+                phase ^= 1u;
+            }
+
+            const uint4 *bp = reinterpret_cast<const uint4 *>(xrow + s * xstride);
+            const uint4 b0l = bp[0], b0h = bp[1], b1l = bp[8], b1h = bp[9];
+            // -(128 + z) as a bf16 pair, for rows gq and gq + 8
+            const uint32_t ncl = ((zb & 0xFu) | 0xC300u) * 0x10001u;
+            const uint32_t nch = ((zb >> 4) | 0xC300u) * 0x10001u;
+            const float sl = __half2float(__ushort_as_half((unsigned short)(sp & 0xFFFFu)));
+            const float sh = __half2float(__ushort_as_half((unsigned short)(sp >> 16)));
+            float d[2][4];
+            chunk_mma<true>(d, w0, b0l, b0h, ncl, nch, zq, nib_mask, bf16_magic);
+            chunk_mma<false>(d, w1, b1l, b1h, ncl, nch, zq, nib_mask, bf16_magic);
+            acc[0] = fmaf(d[0][0] + d[1][0], sl, acc[0]);
+            acc[1] = fmaf(d[0][1] + d[1][1], sl, acc[1]);
+            acc[2] = fmaf(d[0][2] + d[1][2], sh, acc[2]);
+            acc[3] = fmaf(d[0][3] + d[1][3], sh, acc[3]);
+        }
+        if (!ok && lane == 0) atomicOr(err, 1u);
     }
 
+    wait_prerequisites();       // y may be read by the previous kernel in the stream
+    const int t = b * kWarps + warp;
     if (S == 1) {
-        if (active) store_tile<F32OUT>(yv, acc, t, lane, M, N);
+        if (warp < kWarps && ok) store_tile<F32OUT>(yv, acc, t, lane, M, N);
         return;
     }
     // Combine the K slices of the cluster in rank order 0, 1, ..., S-1.
-    float4 *red = reinterpret_cast<float4 *>(reinterpret_cast<char *>(smem) +
-                                             (size_t)(2 * ((G + S - 1) / S)) * M * 128);
-    red[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    float4 *red = reinterpret_cast<float4 *>(smem + plan.red_off);
+    if (warp < kWarps) red[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
-    if (active && (warp % S) == split) {
+    if (warp < kWarps && (warp % S) == split) {
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
         for (int r = 0; r < S; ++r) {
             const float4 v = *cluster.map_shared_rank(&red[warp * 32 + lane], r);
-            s0 += v.x; s1 += v.y; s2 += v.z; s3 += v.w;
+            s0 += v.x;
+            s1 += v.y;
+            s2 += v.z;
+            s3 += v.w;
         }
         const float tot[4] = {s0, s1, s2, s3};
         store_tile<F32OUT>(yv, tot, t, lane, M, N);
@@ -245,29 +401,20 @@ gemv_kernel(const uint4 *__restrict__ qw, const uint32_t *__restrict__ sc,
     cluster.sync();
 }
 
-size_t x_bytes(int K, int S, int M) {
-    const int G = K / kGroup;
-    return (size_t)2 * ((G + S - 1) / S) * M * 128;
-}
-
-size_t smem_bytes(int K, int S, int M) {
-    return x_bytes(K, S, M) + (S > 1 ? (size_t)kWarps * 32 * sizeof(float4) : 0);
-}
-
 }  // namespace
 
 bool gemv_shape(int K, int N, int num_sms, GemvShape *out) {
-    const int T = row_tiles(N);
+    const int NB = row_blocks(N);
     const int G = K / kGroup;
-    const int blocks_n = (T + kWarps - 1) / kWarps;
     const long long slots = 2LL * (num_sms > 0 ? num_sms : 1);
+    const int fill = 2;          // start-up cost of a block, in groups
     int best_s = 0;
     long long best_cost = 0;
     for (int S = 1; S <= kMaxSplits && S <= G; ++S) {
-        if (x_bytes(K, S, W4_MAX_TOKENS) > kMaxXBytes) continue;
-        const long long ctas = (long long)blocks_n * S;
+        if (smem_plan(K, S, W4_MAX_TOKENS, kMinStages).total > kBlockSmemBudget) continue;
+        const long long ctas = (long long)NB * S;
         const long long waves = (ctas + slots - 1) / slots;
-        const long long cost = waves * ((G + S - 1) / S);
+        const long long cost = waves * ((G + S - 1) / S + fill);
         if (best_s == 0 || cost < best_cost) {
             best_s = S;
             best_cost = cost;
@@ -276,43 +423,61 @@ bool gemv_shape(int K, int N, int num_sms, GemvShape *out) {
     if (best_s == 0) return false;
     out->warps = kWarps;
     out->splits = best_s;
+    out->stages = kMinStages;
     return true;
 }
 
 cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zeros,
                         const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
                         const GemvShape &shape, cudaStream_t stream) {
-    const int T = row_tiles(N);
     const int S = shape.splits;
-    const size_t smem = smem_bytes(K, S, M);
+    // The ring is as deep as the shared-memory budget allows for this M (the
+    // depth does not change the arithmetic, so results stay batch-invariant).
+    int stages = kMaxStages;
+    while (stages > kMinStages && smem_plan(K, S, M, stages).total > kBlockSmemBudget) --stages;
+    const SmemPlan plan = smem_plan(K, S, M, stages);
     static bool attr_done[2][64] = {};
     int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
-    if (err != cudaSuccess) return err;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
     auto kern = f32_out ? gemv_kernel<true> : gemv_kernel<false>;
     if (dev < 64 && !attr_done[f32_out][dev]) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)(kMaxXBytes + kWarps * 32 * sizeof(float4)));
-        if (err != cudaSuccess) return err;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kBlockSmemBudget);
+        if (e != cudaSuccess) return e;
         attr_done[f32_out][dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((T + kWarps - 1) / kWarps), (unsigned)S, 1);
-    cfg.blockDim = dim3(kWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.gridDim = dim3((unsigned)row_blocks(N), (unsigned)S, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = plan.total;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = (unsigned)S;
-    attr[0].val.clusterDim.z = 1;
+    // Short (latency-bound) products overlap their start with the tail of the
+    // previous kernel in the stream (programmatic dependent launch); long ones
+    // measured faster without.
+    const bool overlap = (size_t)K * (size_t)N / 2 < kOverlapBelowBytes;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (S > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = (unsigned)S;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (overlap) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = S > 1 ? 1 : 0;
-    const uint4 *qw = reinterpret_cast<const uint4 *>(static_cast<const char *>(qweight) +
-                                                      W4_HEADER_BYTES);
-    return cudaLaunchKernelEx(&cfg, kern, qw, static_cast<const uint32_t *>(scales),
-                              static_cast<const uint8_t *>(zeros),
-                              reinterpret_cast<const uint32_t *>(x), y, M, K, N, T, S);
+    cfg.numAttrs = na;
+    const char *q = static_cast<const char *>(qweight);
+    uint32_t *err = reinterpret_cast<uint32_t *>(const_cast<char *>(q) + kErrorOffset);
+    return cudaLaunchKernelEx(&cfg, kern, q, static_cast<const char *>(scales),
+                              static_cast<const char *>(zeros),
+                              reinterpret_cast<const __nv_bfloat16 *>(x), y, err, M, K, N, S,
+                              stages, 0x000F000Fu, 0x43004300u);
 }
 
 }  // namespace w4

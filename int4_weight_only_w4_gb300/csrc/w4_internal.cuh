@@ -12,7 +12,13 @@ namespace w4 {
 constexpr int kGroup = 128;      // weights per (row, scale, zero) group along K
 constexpr int kTileRows = 16;    // rows per tile = M of one m16n8k16 tensor-core op
 constexpr int kChunkK = 64;      // K covered by one 16-byte load of every lane of a warp
+constexpr int kBlockTiles = 8;   // tiles per row block (one per consumer warp)
+constexpr int kBlockRows = kTileRows * kBlockTiles;   // 128
 constexpr int kMaxSplits = 8;    // thread blocks per cluster (portable cluster size)
+// Bytes of one (row block, group) record in each of the three buffers.
+constexpr int kRecWeights = kBlockTiles * 1024;      // 8 tiles x 2 chunks x 32 lanes x 16 B
+constexpr int kRecScales = kBlockTiles * 8 * 4;      // 8 tiles x 8 lane groups x 2 fp16
+constexpr int kRecZeros = kBlockTiles * 8;           // 8 tiles x 8 lane groups x 2 nibbles
 
 // First W4_HEADER_BYTES of a repacked qweight buffer.
 struct Header {
@@ -22,21 +28,23 @@ struct Header {
     int32_t K;
     int32_t N;
     uint32_t bad_zeros;     // set by w4_repack when a zero point > 15 was seen
-    uint32_t reserved[25];
+    uint32_t kernel_error;  // set by w4_gemv if a wait gave up (never in normal operation)
+    uint32_t reserved[24];
 };
 static_assert(sizeof(Header) == W4_HEADER_BYTES, "header size");
 
-inline int row_tiles(int N) { return (N + kTileRows - 1) / kTileRows; }
+inline int row_blocks(int N) { return (N + kBlockRows - 1) / kBlockRows; }
+constexpr size_t kErrorOffset = 28;   // byte offset of Header::kernel_error
 
 // Kernel-layout byte sizes (see w4_repack.cu for the layout itself).
 inline size_t packed_qweight_bytes(int K, int N) {
-    return (size_t)W4_HEADER_BYTES + (size_t)row_tiles(N) * kTileRows * (size_t)K / 2;
+    return (size_t)W4_HEADER_BYTES + (size_t)row_blocks(N) * (K / kGroup) * kRecWeights;
 }
 inline size_t packed_scales_bytes(int K, int N) {
-    return (size_t)row_tiles(N) * (K / kGroup) * 8 * sizeof(uint32_t);
+    return (size_t)row_blocks(N) * (K / kGroup) * kRecScales;
 }
 inline size_t packed_zeros_bytes(int K, int N) {
-    return (size_t)row_tiles(N) * (K / kGroup) * 8;
+    return (size_t)row_blocks(N) * (K / kGroup) * kRecZeros;
 }
 
 cudaError_t launch_repack(const uint32_t *qweight, const uint16_t *scales,
@@ -48,8 +56,9 @@ cudaError_t launch_dequant(const uint32_t *qweight, const uint16_t *scales,
                            cudaStream_t stream);
 
 struct GemvShape {
-    int warps;    // warps per block; each owns one 16-row tile
+    int warps;    // consumer warps per block; each owns one 16-row tile
     int splits;   // K splits = blocks per cluster
+    int stages;   // depth of the shared-memory weight ring
 };
 
 // Launch shape for an N x K weight (independent of M).  Returns false if no

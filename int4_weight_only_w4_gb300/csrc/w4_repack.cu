@@ -2,25 +2,30 @@
 //
 // The kernel layout feeds the bf16 tensor-core operation mma.m16n8k16 with
 // weights as its A operand (16 rows x 16 k) and up to 8 tokens as its B
-// operand.  Rows are grouped in tiles of 16; K in chunks of 64.  For tile t
-// and chunk c, lane l = 4*gq + tq of a warp loads the 16 bytes
-//     qweight_out + 128 + ((t * K/64 + c) * 32 + l) * 16
-// i.e. four 32-bit words, one per 16-wide k-step j = 0..3 (kb = 64c + 16j).
-// Word j holds the eight nibbles that lane owns in the A fragment of that
-// step, arranged so that (word >> 4p) & 0x000F000F gives A register p as a
-// pair (low half: even k, high half: odd k):
-//     bits  0- 3 / 16-19 : row 16t+gq,   k = kb+2tq / kb+2tq+1    (register 0)
-//     bits  4- 7 / 20-23 : row 16t+gq+8, k = kb+2tq / kb+2tq+1    (register 1)
-//     bits  8-11 / 24-27 : row 16t+gq,   k = kb+2tq+8 / +9        (register 2)
-//     bits 12-15 / 28-31 : row 16t+gq+8, k = kb+2tq+8 / +9        (register 3)
-// This is the even/odd pair interleave of "Building an LLM Inference Runtime
-// ...", section "Bug #3" (nibble slots hold w0,w2,w4,w6 in the low half-word
-// and w1,w3,w5,w7 in the high one), extended to the two rows of a fragment.
-//
-// Scales: [tile][group][gq] uint32 = fp16 scale of row 16t+gq (low half) and of
-// row 16t+gq+8 (high half).  Zeros: [tile][group][gq] byte = z of row 16t+gq
-// (low nibble) | z of row 16t+gq+8 (high nibble).  Rows past N are padded
-// with q = z = 0 and s = 0, so they contribute exact zeros.
+// operand, and is cut into records that one bulk copy can move: rows are
+// grouped in tiles of 16 and row blocks of 8 tiles (128 rows, padded with
+// zero weights past N); K in groups of 128.  Record (b, g) -- row block b,
+// group g -- holds, in each of the three buffers:
+//   qweight: 8 KB at 128 + (b*G + g) * 8192: tile w (0..7), chunk c (0..1,
+//            64 k each), lane l = 4*gq + tq: 16 bytes at w*1024 + c*512 + l*16,
+//            four 32-bit words, one per 16-wide k-step j = 0..3
+//            (kb = 128g + 64c + 16j).  Word j holds the eight nibbles that lane
+//            owns in the A fragment of that step, arranged so that
+//            (word >> 4p) & 0x000F000F gives A register p as a pair (low half:
+//            even k, high half: odd k):
+//              bits  0- 3 / 16-19 : row 16t+gq,   k = kb+2tq / kb+2tq+1   (reg 0)
+//              bits  4- 7 / 20-23 : row 16t+gq+8, k = kb+2tq / kb+2tq+1   (reg 1)
+//              bits  8-11 / 24-27 : row 16t+gq,   k = kb+2tq+8 / +9       (reg 2)
+//              bits 12-15 / 28-31 : row 16t+gq+8, k = kb+2tq+8 / +9       (reg 3)
+//            with t = 8b + w.  This is the even/odd pair interleave of
+//            "Building an LLM Inference Runtime ...", section "Bug #3" (nibble
+//            slots hold w0,w2,w4,w6 in the low half-word and w1,w3,w5,w7 in the
+//            high one), extended to the two rows of a fragment.
+//   scales:  256 B at (b*G + g) * 256: uint32 [w][gq] = fp16 scale of row
+//            16t+gq (low half) and of row 16t+gq+8 (high half).
+//   zeros:   64 B at (b*G + g) * 64: byte [w][gq] = z of row 16t+gq (low
+//            nibble) | z of row 16t+gq+8 (high nibble).
+// Padded rows have q = z = 0 and s = 0, so they contribute exact zeros.
 #include <string.h>
 
 #include "w4_internal.cuh"
@@ -36,32 +41,35 @@ __global__ void write_header_kernel(Header *h, int K, int N) {
     h->K = K;
     h->N = N;
     h->bad_zeros = 0;
-    for (int i = 0; i < 25; ++i) h->reserved[i] = 0;
+    h->kernel_error = 0;
+    for (int i = 0; i < 24; ++i) h->reserved[i] = 0;
 }
 
 __device__ __forceinline__ uint32_t nib(uint32_t w, int i) { return (w >> (4 * i)) & 0xFu; }
 
-__global__ void repack_weights_kernel(const uint32_t *__restrict__ qw, int K, int N, int T,
+__global__ void repack_weights_kernel(const uint32_t *__restrict__ qw, int K, int N, int NB,
                                       uint4 *__restrict__ out) {
-    const int C = K / kChunkK;
+    const int G = K / kGroup;
     const size_t words_per_row = (size_t)K / 8;
-    const size_t total = (size_t)T * C * 32;
+    const size_t total = (size_t)NB * G * (kRecWeights / 16);
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
         const int lane = (int)(i & 31);
-        const size_t tc = i >> 5;
-        const int c = (int)(tc % C);
-        const int t = (int)(tc / C);
+        const int c = (int)((i >> 5) & 1);
+        const int w = (int)((i >> 6) & 7);
+        const size_t bg = i >> 9;
+        const int g = (int)(bg % G);
+        const int b = (int)(bg / G);
         const int gq = lane >> 2, tq = lane & 3;
-        const int r0 = t * kTileRows + gq, r1 = r0 + 8;
+        const int r0 = (b * kBlockTiles + w) * kTileRows + gq, r1 = r0 + 8;
         uint32_t res[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const size_t w = (size_t)(c * kChunkK + j * 16) / 8;   // canonical word of k = kb
-            const uint32_t a0 = r0 < N ? qw[r0 * words_per_row + w] : 0u;
-            const uint32_t b0 = r0 < N ? qw[r0 * words_per_row + w + 1] : 0u;
-            const uint32_t a1 = r1 < N ? qw[r1 * words_per_row + w] : 0u;
-            const uint32_t b1 = r1 < N ? qw[r1 * words_per_row + w + 1] : 0u;
+            const size_t wd = (size_t)(g * kGroup + c * kChunkK + j * 16) / 8;  // word of k = kb
+            const uint32_t a0 = r0 < N ? qw[r0 * words_per_row + wd] : 0u;
+            const uint32_t b0 = r0 < N ? qw[r0 * words_per_row + wd + 1] : 0u;
+            const uint32_t a1 = r1 < N ? qw[r1 * words_per_row + wd] : 0u;
+            const uint32_t b1 = r1 < N ? qw[r1 * words_per_row + wd + 1] : 0u;
             const int e = 2 * tq, o = 2 * tq + 1;       // nibble slots of k = kb+2tq, kb+2tq+1
             res[j] = nib(a0, e) | (nib(a1, e) << 4) | (nib(b0, e) << 8) | (nib(b1, e) << 12) |
                      (nib(a0, o) << 16) | (nib(a1, o) << 20) | (nib(b0, o) << 24) |
@@ -72,21 +80,22 @@ __global__ void repack_weights_kernel(const uint32_t *__restrict__ qw, int K, in
 }
 
 __global__ void repack_meta_kernel(const uint16_t *__restrict__ sc, const uint8_t *__restrict__ zp,
-                                   int K, int N, int T, uint32_t *__restrict__ sc_out,
+                                   int K, int N, int NB, uint32_t *__restrict__ sc_out,
                                    uint8_t *__restrict__ zp_out, Header *h) {
     const int G = K / kGroup;
-    const size_t total = (size_t)T * G * 8;
+    const size_t total = (size_t)NB * G * 64;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (size_t)gridDim.x * blockDim.x) {
         const int gq = (int)(i & 7);
-        const size_t tg = i >> 3;
-        const int gi = (int)(tg % G);
-        const int t = (int)(tg / G);
-        const int r0 = t * kTileRows + gq, r1 = r0 + 8;
-        const uint32_t s0 = r0 < N ? sc[(size_t)r0 * G + gi] : 0u;
-        const uint32_t s1 = r1 < N ? sc[(size_t)r1 * G + gi] : 0u;
-        const uint32_t z0 = r0 < N ? zp[(size_t)r0 * G + gi] : 0u;
-        const uint32_t z1 = r1 < N ? zp[(size_t)r1 * G + gi] : 0u;
+        const int w = (int)((i >> 3) & 7);
+        const size_t bg = i >> 6;
+        const int g = (int)(bg % G);
+        const int b = (int)(bg / G);
+        const int r0 = (b * kBlockTiles + w) * kTileRows + gq, r1 = r0 + 8;
+        const uint32_t s0 = r0 < N ? sc[(size_t)r0 * G + g] : 0u;
+        const uint32_t s1 = r1 < N ? sc[(size_t)r1 * G + g] : 0u;
+        const uint32_t z0 = r0 < N ? zp[(size_t)r0 * G + g] : 0u;
+        const uint32_t z1 = r1 < N ? zp[(size_t)r1 * G + g] : 0u;
         if (z0 > 15u || z1 > 15u) atomicOr(&h->bad_zeros, 1u);
         sc_out[i] = s0 | (s1 << 16);
         zp_out[i] = (uint8_t)((z0 & 0xFu) | ((z1 & 0xFu) << 4));
@@ -104,16 +113,17 @@ int grid_for(size_t work, int threads) {
 cudaError_t launch_repack(const uint32_t *qweight, const uint16_t *scales, const uint8_t *zeros,
                           int K, int N, void *qweight_out, void *scales_out, void *zeros_out,
                           cudaStream_t stream) {
-    const int T = row_tiles(N);
+    const int NB = row_blocks(N);
+    const int G = K / kGroup;
     Header *h = static_cast<Header *>(qweight_out);
     write_header_kernel<<<1, 1, 0, stream>>>(h, K, N);
-    const size_t lanes = (size_t)T * (K / kChunkK) * 32;
-    repack_weights_kernel<<<grid_for(lanes, 256), 256, 0, stream>>>(
-        qweight, K, N, T,
+    const size_t pieces = (size_t)NB * G * (kRecWeights / 16);
+    repack_weights_kernel<<<grid_for(pieces, 256), 256, 0, stream>>>(
+        qweight, K, N, NB,
         reinterpret_cast<uint4 *>(static_cast<char *>(qweight_out) + W4_HEADER_BYTES));
-    const size_t metas = (size_t)T * (K / kGroup) * 8;
+    const size_t metas = (size_t)NB * G * 64;
     repack_meta_kernel<<<grid_for(metas, 256), 256, 0, stream>>>(
-        scales, zeros, K, N, T, static_cast<uint32_t *>(scales_out),
+        scales, zeros, K, N, NB, static_cast<uint32_t *>(scales_out),
         static_cast<uint8_t *>(zeros_out), h);
     return cudaGetLastError();
 }

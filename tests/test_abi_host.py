@@ -58,11 +58,11 @@ def sizes(lib, K, N):
 @pytest.mark.parametrize("K,N", [(128, 1), (3584, 37888), (18944, 3584), (256, 17)])
 def test_repacked_sizes(lib, K, N):
     st, q, s, z = sizes(lib, K, N)
-    tiles = (N + 15) // 16
+    blocks = (N + 127) // 128
     assert st == 0
-    assert q == 128 + tiles * 16 * K // 2
-    assert s == tiles * (K // 128) * 8 * 4
-    assert z == tiles * (K // 128) * 8
+    assert q == 128 + blocks * (K // 128) * 8192
+    assert s == blocks * (K // 128) * 256
+    assert z == blocks * (K // 128) * 64
 
 
 @pytest.mark.parametrize("K,N", [(0, 8), (100, 8), (128, 0), (-128, 4)])
@@ -82,8 +82,8 @@ def gemv(lib, q=FAKE, s=FAKE, z=FAKE, x=FAKE, y=FAKE, M=1, K=128, N=16):
 @pytest.mark.parametrize("kw,want", [
     (dict(q=None), 1), (dict(s=None), 1), (dict(z=None), 1), (dict(x=None), 1),
     (dict(y=None), 1), (dict(K=100), 1), (dict(K=0), 1), (dict(N=0), 1),
-    (dict(M=0), 2), (dict(M=9), 2), (dict(q=FAKE + 8), 1), (dict(s=FAKE + 2), 1),
-    (dict(x=FAKE + 2), 1), (dict(y=FAKE + 1), 1),
+    (dict(M=0), 2), (dict(M=9), 2), (dict(q=FAKE + 8), 1), (dict(s=FAKE + 4), 1),
+    (dict(z=FAKE + 8), 1), (dict(x=FAKE + 8), 1), (dict(y=FAKE + 1), 1),
 ])
 def test_gemv_argument_errors(lib, kw, want):
     assert gemv(lib, **kw) == want
@@ -100,13 +100,13 @@ def test_dequant_and_repack_argument_errors(lib):
     assert lib.w4_repack(FAKE, FAKE, FAKE, 64, 4, FAKE, FAKE, FAKE, None) == 1
 
 
-def header(K, N, magic=b"W4G128KL", layout=1, version=1, bad=0):
-    return magic + struct.pack("<IIiiI", layout, version, K, N, bad) + bytes(100)
+def header(K, N, magic=b"W4G128KL", layout=1, version=2, bad=0, kerr=0):
+    return magic + struct.pack("<IIiiII", layout, version, K, N, bad, kerr) + bytes(96)
 
 
 @pytest.mark.parametrize("mut,want", [
     (dict(), 0), (dict(magic=b"W4G128XX"), 3), (dict(layout=2), 3), (dict(version=9), 3),
-    (dict(K=256), 3), (dict(N=17), 3), (dict(bad=1), 3),
+    (dict(K=256), 3), (dict(N=17), 3), (dict(bad=1), 3), (dict(kerr=1), 4),
 ])
 def test_check_header(lib, mut, want):
     args = dict(K=384, N=64)
