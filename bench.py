@@ -52,6 +52,21 @@ def chain_bytes(layers: int = syn.LAYERS_7B, M: int = 1) -> int:
     return layers * sum(canonical_bytes(M, K, N) for _, K, N in syn.LAYER_7B)
 
 
+def gemv_traffic():
+    """DRAM bytes per gate_up launch from the committed ncu summary, or None
+    when the kernel source has changed since those counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemv_traffic.json")) as f:
+            rec = json.load(f)
+        with open(os.path.join(ROOT, "int4_weight_only_w4_gb300", "csrc", "w4_gemv.cu"),
+                  "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        return rec["traffic_bytes_per_launch"] if sha == rec["w4_gemv_cu_sha256_16"] else None
+    except Exception:
+        return None
+
+
 def read_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -77,10 +92,14 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.reader = threading.Thread(target=self._read, daemon=True)
             self.reader.start()
+            t0 = time.time()                 # start timing only once sampling runs
+            while not self.lines and time.time() - t0 < 10 and self.proc.poll() is None:
+                time.sleep(0.01)
+            self.first = len(self.lines)
         except Exception:
             self.proc = None
         return self
@@ -339,7 +358,8 @@ def gpu_arm(args):
             "peak_hbm_gbs": peak, "peak_kind": peak_kind,
             "frac_of_nominal_8tbs": round(value / world / 8000.0, 4),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
-                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": gemv_traffic(),
                          "kernel": "w4 gemv, gate_up 3584->37888, M=1",
                          "bytes_per_launch": gu_bytes,
                          "launch_us": round(gu_launch_us, 3), "peak_kind": peak_kind},
@@ -440,7 +460,7 @@ def per_shape_arm(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["w4", "reference"], default="w4")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
