@@ -58,7 +58,7 @@ typedef enum w4_status {
 #define W4_GROUP_SIZE 128
 #define W4_MAX_TOKENS 8
 #define W4_LAYOUT_ID 1
-#define W4_LAYOUT_VERSION 2
+#define W4_LAYOUT_VERSION 3
 #define W4_HEADER_BYTES 128
 
 /* Human-readable name of a status code (static string, never NULL). */

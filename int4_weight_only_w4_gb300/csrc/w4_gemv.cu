@@ -54,6 +54,7 @@ constexpr int kStageBytes = kRecWeights + kRecScales + kRecZeros;   // 8512
 constexpr int kMinStages = 4;                       // ring depth the split choice assumes
 constexpr int kMaxStages = 12;                      // deepest ring a launch uses
 constexpr size_t kBlockSmemBudget = 113 * 1024;     // two blocks per SM
+constexpr size_t kBlockSmemBudget3 = 74 * 1024;     // three blocks per SM (small M)
 constexpr long long kWaitLimit = 4000000000LL;      // clock cycles (~2 s)
 constexpr size_t kOverlapBelowBytes = 16u << 20;    // packed weights of a "short" product
 
@@ -161,7 +162,9 @@ __device__ __forceinline__ void consumer_sync() {
 
 // One 64-k chunk: four k-steps j; steps 0, 1 go to accumulator d[0] and steps
 // 2, 3 to d[1] (two independent chains).  bl, bh hold this lane's eight B
-// registers for the chunk (pairs (k, k+1) and (k+8, k+9) of each step).
+// registers for the chunk: x pairs 8tq .. 8tq+7 of the chunk, register 2j
+// for the step's first column pair and 2j+1 for its second (the permuted k
+// order of w4_repack.cu).
 // ncl, nch = -(128 + z) for rows gq and gq + 8 as bf16 pairs.  mask and magic
 // are 0x000F000F and 0x43004300, passed in registers so that each extraction
 // is one three-input logic operation.  FIRST: the accumulators start from zero.
@@ -189,6 +192,43 @@ __device__ __forceinline__ void chunk_mma(float (&d)[2][4], const uint4 &w, cons
     }
 }
 
+// What a consumer lane takes out of one stage: its two 16-byte weight pieces,
+// the scale pair of its rows and their zero-point pair.
+struct GroupData {
+    uint4 w0, w1;
+    uint32_t sp, zb;
+};
+
+__device__ __forceinline__ GroupData read_group(const unsigned char *st, int warp, int lane) {
+    GroupData g;
+    g.w0 = *reinterpret_cast<const uint4 *>(st + warp * 1024 + lane * 16);
+    g.w1 = *reinterpret_cast<const uint4 *>(st + warp * 1024 + 512 + lane * 16);
+    g.sp = *reinterpret_cast<const uint32_t *>(st + kRecWeights + warp * 32 + (lane >> 2) * 4);
+    g.zb = st[kRecWeights + kRecScales + warp * 8 + (lane >> 2)];
+    return g;
+}
+
+// One group (two 64-k chunks) into the lane's four fp32 accumulators:
+// acc += s * sum_group (q - z) x for its two rows and two token columns.
+__device__ __forceinline__ void group_mma(float (&acc)[4], const GroupData &g,
+                                          const uint32_t *xg, const float (&zq)[4],
+                                          uint32_t mask, uint32_t magic) {
+    const uint4 *bp = reinterpret_cast<const uint4 *>(xg);
+    const uint4 b0l = bp[0], b0h = bp[1], b1l = bp[8], b1h = bp[9];
+    // -(128 + z) as a bf16 pair, for rows gq and gq + 8
+    const uint32_t ncl = ((g.zb & 0xFu) | 0xC300u) * 0x10001u;
+    const uint32_t nch = ((g.zb >> 4) | 0xC300u) * 0x10001u;
+    const float sl = __half2float(__ushort_as_half((unsigned short)(g.sp & 0xFFFFu)));
+    const float sh = __half2float(__ushort_as_half((unsigned short)(g.sp >> 16)));
+    float d[2][4];
+    chunk_mma<true>(d, g.w0, b0l, b0h, ncl, nch, zq, mask, magic);
+    chunk_mma<false>(d, g.w1, b1l, b1h, ncl, nch, zq, mask, magic);
+    acc[0] = fmaf(d[0][0] + d[1][0], sl, acc[0]);
+    acc[1] = fmaf(d[0][1] + d[1][1], sl, acc[1]);
+    acc[2] = fmaf(d[0][2] + d[1][2], sh, acc[2]);
+    acc[3] = fmaf(d[0][3] + d[1][3], sh, acc[3]);
+}
+
 template <bool F32OUT>
 __device__ __forceinline__ void store_tile(void *yv, const float (&acc)[4], int t, int lane,
                                            int M, int N) {
@@ -213,8 +253,8 @@ struct SmemPlan {
     size_t x_off, x_row_bytes, zero_off, red_off, bar_off, total;
 };
 
-// Shared memory: [stages][weights | scales | zeros] [x rows, permuted in place
-// into B-fragment order] [256 zero bytes] [partials] [barriers]
+// Shared memory: [stages][weights | scales | zeros] [x rows as copied]
+// [256 zero bytes] [partials] [barriers]
 __host__ __device__ inline SmemPlan smem_plan(int K, int S, int M, int stages) {
     const int G = K / kGroup;
     const int gmax = (G + S - 1) / S;
@@ -228,8 +268,8 @@ __host__ __device__ inline SmemPlan smem_plan(int K, int S, int M, int stages) {
     return p;
 }
 
-template <bool F32OUT>
-__global__ void __launch_bounds__(kThreads, 2)
+template <bool F32OUT, int MIN_BLOCKS>
+__global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
 gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             const char *__restrict__ zp, const __nv_bfloat16 *__restrict__ x,
             void *__restrict__ yv, uint32_t *err, int M, int K, int N, int S, int stages,
@@ -318,23 +358,15 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
         // Token columns >= M read a 256-byte zero patch at a fixed address.
         uint32_t *zpatch = reinterpret_cast<uint32_t *>(smem + plan.zero_off);
         if (threadIdx.x < 64) zpatch[threadIdx.x] = 0u;
-        // Wait for x, then permute each 64-k segment of each token row in place
-        // (one warp per segment): word u of the segment (k = 64c + 2u, step
-        // j = u / 8, o = u % 8) moves to (o % 4) * 8 + 2j + o / 4, so that lane tq
-        // finds its eight B registers for the chunk as two 16-byte words.
-        if (!mbar_wait(xbar, 0)) ok = false;
-        for (int seg = warp; seg < M * ng * 2; seg += kWarps) {
-            const int m = seg / (ng * 2), c = seg - m * (ng * 2);
-            uint32_t *row = reinterpret_cast<uint32_t *>(xs + (size_t)m * plan.x_row_bytes) + c * 32;
-            const uint32_t v = row[lane];
-            __syncwarp();
-            row[(lane & 3) * 8 + 2 * (lane >> 3) + ((lane >> 2) & 1)] = v;
-        }
         consumer_sync();
+        // x is used as copied: the kernel layout orders k inside each 64-k chunk
+        // so that lane tq's eight B registers are the x pairs at
+        // 64c + 16tq .. 64c + 16tq + 15 (see w4_repack.cu).
+        if (!mbar_wait(xbar, 0)) ok = false;
         const bool has_x = gq < M;
         const uint32_t *xrow =
             (has_x ? reinterpret_cast<const uint32_t *>(xs + (size_t)gq * plan.x_row_bytes)
-                   : zpatch) + tq * 8;
+                   : zpatch) + tq * 8;   // words 8tq .. 8tq+7 of each 32-word chunk
         const int xstride = has_x ? 64 : 0;     // words per group
         const float zq[4] = {0.f, 0.f, 0.f, 0.f};
         int slot = 0;
@@ -344,33 +376,14 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
                 ok = false;
                 break;
             }
-            const unsigned char *st = smem + (size_t)slot * kStageBytes;
-            const uint4 w0 = *reinterpret_cast<const uint4 *>(st + warp * 1024 + lane * 16);
-            const uint4 w1 = *reinterpret_cast<const uint4 *>(st + warp * 1024 + 512 + lane * 16);
-            const uint32_t sp =
-                *reinterpret_cast<const uint32_t *>(st + kRecWeights + warp * 32 + gq * 4);
-            const uint32_t zb = st[kRecWeights + kRecScales + warp * 8 + gq];
+            const GroupData g = read_group(smem + (size_t)slot * kStageBytes, warp, lane);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (lane == 0) mbar_arrive(&empty[slot]);    // stage copied to registers
             if (++slot == stages) {
                 slot = 0;
                 phase ^= 1u;
             }
-
-            const uint4 *bp = reinterpret_cast<const uint4 *>(xrow + s * xstride);
-            const uint4 b0l = bp[0], b0h = bp[1], b1l = bp[8], b1h = bp[9];
-            // -(128 + z) as a bf16 pair, for rows gq and gq + 8
-            const uint32_t ncl = ((zb & 0xFu) | 0xC300u) * 0x10001u;
-            const uint32_t nch = ((zb >> 4) | 0xC300u) * 0x10001u;
-            const float sl = __half2float(__ushort_as_half((unsigned short)(sp & 0xFFFFu)));
-            const float sh = __half2float(__ushort_as_half((unsigned short)(sp >> 16)));
-            float d[2][4];
-            chunk_mma<true>(d, w0, b0l, b0h, ncl, nch, zq, nib_mask, bf16_magic);
-            chunk_mma<false>(d, w1, b1l, b1h, ncl, nch, zq, nib_mask, bf16_magic);
-            acc[0] = fmaf(d[0][0] + d[1][0], sl, acc[0]);
-            acc[1] = fmaf(d[0][1] + d[1][1], sl, acc[1]);
-            acc[2] = fmaf(d[0][2] + d[1][2], sh, acc[2]);
-            acc[3] = fmaf(d[0][3] + d[1][3], sh, acc[3]);
+            group_mma(acc, g, xrow + s * xstride, zq, nib_mask, bf16_magic);
         }
         if (!ok && lane == 0) atomicOr(err, 1u);
     }
@@ -435,17 +448,25 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     // depth does not change the arithmetic, so results stay batch-invariant).
     int stages = kMaxStages;
     while (stages > kMinStages && smem_plan(K, S, M, stages).total > kBlockSmemBudget) --stages;
+    // Small M: x is small, so three blocks fit per SM (more warps to hide
+    // latency).  The split S, and so the arithmetic, is the same either way.
+    int stages3 = kMaxStages;
+    while (stages3 > kMinStages && smem_plan(K, S, M, stages3).total > kBlockSmemBudget3)
+        --stages3;
+    const bool three = M <= 2 && smem_plan(K, S, M, stages3).total <= kBlockSmemBudget3;
+    if (three) stages = stages3;
     const SmemPlan plan = smem_plan(K, S, M, stages);
-    static bool attr_done[2][64] = {};
+    static bool attr_done[2][2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    auto kern = f32_out ? gemv_kernel<true> : gemv_kernel<false>;
-    if (dev < 64 && !attr_done[f32_out][dev]) {
+    auto kern = f32_out ? (three ? gemv_kernel<true, 3> : gemv_kernel<true, 2>)
+                        : (three ? gemv_kernel<false, 3> : gemv_kernel<false, 2>);
+    if (dev < 64 && !attr_done[f32_out][three][dev]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kBlockSmemBudget);
+                                 (int)(three ? kBlockSmemBudget3 : kBlockSmemBudget));
         if (e != cudaSuccess) return e;
-        attr_done[f32_out][dev] = true;
+        attr_done[f32_out][three][dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)row_blocks(N), (unsigned)S, 1);

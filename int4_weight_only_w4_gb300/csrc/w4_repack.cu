@@ -7,20 +7,27 @@
 // zero weights past N); K in groups of 128.  Record (b, g) -- row block b,
 // group g -- holds, in each of the three buffers:
 //   qweight: 8 KB at 128 + (b*G + g) * 8192: tile w (0..7), chunk c (0..1,
-//            64 k each), lane l = 4*gq + tq: 16 bytes at w*1024 + c*512 + l*16,
-//            four 32-bit words, one per 16-wide k-step j = 0..3
-//            (kb = 128g + 64c + 16j).  Word j holds the eight nibbles that lane
-//            owns in the A fragment of that step, arranged so that
-//            (word >> 4p) & 0x000F000F gives A register p as a pair (low half:
-//            even k, high half: odd k):
-//              bits  0- 3 / 16-19 : row 16t+gq,   k = kb+2tq / kb+2tq+1   (reg 0)
-//              bits  4- 7 / 20-23 : row 16t+gq+8, k = kb+2tq / kb+2tq+1   (reg 1)
-//              bits  8-11 / 24-27 : row 16t+gq,   k = kb+2tq+8 / +9       (reg 2)
-//              bits 12-15 / 28-31 : row 16t+gq+8, k = kb+2tq+8 / +9       (reg 3)
-//            with t = 8b + w.  This is the even/odd pair interleave of
-//            "Building an LLM Inference Runtime ...", section "Bug #3" (nibble
-//            slots hold w0,w2,w4,w6 in the low half-word and w1,w3,w5,w7 in the
-//            high one), extended to the two rows of a fragment.
+//            64 k each, kc = 128g + 64c), lane l = 4*gq + tq: 16 bytes at
+//            w*1024 + c*512 + l*16, four 32-bit words, one per k-step j = 0..3
+//            of the tensor-core operation.  The sum over k does not depend on
+//            the order of k, so inside a chunk the k-steps take a permuted k:
+//            column pair (2tq, 2tq+1) of step j is k = kc + 16tq + 4j + {0, 1}
+//            and column pair (2tq+8, 2tq+9) is k = kc + 16tq + 4j + {2, 3}.
+//            With that order the B registers a lane needs for the chunk are
+//            the eight consecutive x pairs starting at kc + 16tq: two 16-byte
+//            loads straight from x as copied, no rearranging.  Word j holds
+//            the eight nibbles the lane owns in the A fragment of step j,
+//            arranged so that (word >> 4p) & 0x000F000F gives A register p as
+//            a pair (low half: the first k of the pair, high half: the second):
+//              bits  0- 3 / 16-19 : row 16t+gq,   k = kk+0 / kk+1   (reg 0)
+//              bits  4- 7 / 20-23 : row 16t+gq+8, k = kk+0 / kk+1   (reg 1)
+//              bits  8-11 / 24-27 : row 16t+gq,   k = kk+2 / kk+3   (reg 2)
+//              bits 12-15 / 28-31 : row 16t+gq+8, k = kk+2 / kk+3   (reg 3)
+//            with t = 8b + w and kk = kc + 16tq + 4j.  This is the even/odd
+//            pair interleave of "Building an LLM Inference Runtime ...",
+//            section "Bug #3" (nibble slots hold w0,w2,w4,w6 in the low
+//            half-word and w1,w3,w5,w7 in the high one), extended to the two
+//            rows of a fragment.
 //   scales:  256 B at (b*G + g) * 256: uint32 [w][gq] = fp16 scale of row
 //            16t+gq (low half) and of row 16t+gq+8 (high half).
 //   zeros:   64 B at (b*G + g) * 64: byte [w][gq] = z of row 16t+gq (low
@@ -65,15 +72,14 @@ __global__ void repack_weights_kernel(const uint32_t *__restrict__ qw, int K, in
         uint32_t res[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const size_t wd = (size_t)(g * kGroup + c * kChunkK + j * 16) / 8;  // word of k = kb
-            const uint32_t a0 = r0 < N ? qw[r0 * words_per_row + wd] : 0u;
-            const uint32_t b0 = r0 < N ? qw[r0 * words_per_row + wd + 1] : 0u;
-            const uint32_t a1 = r1 < N ? qw[r1 * words_per_row + wd] : 0u;
-            const uint32_t b1 = r1 < N ? qw[r1 * words_per_row + wd + 1] : 0u;
-            const int e = 2 * tq, o = 2 * tq + 1;       // nibble slots of k = kb+2tq, kb+2tq+1
-            res[j] = nib(a0, e) | (nib(a1, e) << 4) | (nib(b0, e) << 8) | (nib(b1, e) << 12) |
-                     (nib(a0, o) << 16) | (nib(a1, o) << 20) | (nib(b0, o) << 24) |
-                     (nib(b1, o) << 28);
+            const int kk = g * kGroup + c * kChunkK + 16 * tq + 4 * j;   // four k: kk .. kk+3
+            const size_t wd = (size_t)kk / 8;                           // canonical word
+            const int o = kk % 8;                                       // first nibble slot
+            const uint32_t a = r0 < N ? qw[r0 * words_per_row + wd] : 0u;
+            const uint32_t b = r1 < N ? qw[r1 * words_per_row + wd] : 0u;
+            res[j] = nib(a, o) | (nib(b, o) << 4) | (nib(a, o + 2) << 8) |
+                     (nib(b, o + 2) << 12) | (nib(a, o + 1) << 16) | (nib(b, o + 1) << 20) |
+                     (nib(a, o + 3) << 24) | (nib(b, o + 3) << 28);
         }
         out[i] = make_uint4(res[0], res[1], res[2], res[3]);
     }
