@@ -421,14 +421,18 @@ bool gemv_shape(int K, int N, int num_sms, GemvShape *out) {
     const int G = K / kGroup;
     const long long slots = 2LL * (num_sms > 0 ? num_sms : 1);
     const int fill = 2;          // start-up cost of a block, in groups
+    // Cluster sizes 3, 5 and 7 measured slower than their neighbours on
+    // GB300 (clusters of those sizes pack unevenly onto the SMs of a GPC).
+    static const int kCandidates[] = {1, 2, 4, 6, 8};
     int best_s = 0;
     long long best_cost = 0;
-    for (int S = 1; S <= kMaxSplits && S <= G; ++S) {
+    for (int S : kCandidates) {
+        if (S > G || S > kMaxSplits) continue;
         if (smem_plan(K, S, W4_MAX_TOKENS, kMinStages).total > kBlockSmemBudget) continue;
         const long long ctas = (long long)NB * S;
         const long long waves = (ctas + slots - 1) / slots;
         const long long cost = waves * ((G + S - 1) / S + fill);
-        if (best_s == 0 || cost < best_cost) {
+        if (best_s == 0 || cost <= best_cost) {
             best_s = S;
             best_cost = cost;
         }
