@@ -14,8 +14,8 @@
 // completion counted in bytes on an mbarrier), and the block's K slice of x
 // once at the start.  Eight consumer warps (one per 16-row tile) wait on a
 // stage's "full" barrier, copy their part of it into registers and release it
-// on the stage's "empty" barrier, so the producer keeps `stages` groups (up
-// to ~50 KB per block) in flight: the copy engine, not per-thread loads,
+// on the stage's "empty" barrier, so the producer keeps kStages groups (51 KB
+// per block) in flight: the copy engine, not per-thread loads,
 // carries the bytes in flight that HBM needs.  This is the one-producer,
 // several-consumers, transaction-counted-barrier arrangement of "Building an
 // LLM Inference Runtime ...", section "Bug #1", applied to weight streaming.
@@ -51,8 +51,7 @@ namespace {
 constexpr int kWarps = kBlockTiles;                 // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;         // + one producer warp
 constexpr int kStageBytes = kRecWeights + kRecScales + kRecZeros;   // 8512
-constexpr int kMinStages = 4;                       // ring depth the split choice assumes
-constexpr int kMaxStages = 12;                      // deepest ring a launch uses
+constexpr int kStages = 6;                          // shared-memory ring depth
 constexpr size_t kBlockSmemBudget = 113 * 1024;     // two blocks per SM
 constexpr size_t kBlockSmemBudget3 = 74 * 1024;     // three blocks per SM (small M)
 constexpr long long kWaitLimit = 4000000000LL;      // clock cycles (~2 s)
@@ -255,16 +254,16 @@ struct SmemPlan {
 
 // Shared memory: [stages][weights | scales | zeros] [x rows as copied]
 // [256 zero bytes] [partials] [barriers]
-__host__ __device__ inline SmemPlan smem_plan(int K, int S, int M, int stages) {
+__host__ __device__ inline SmemPlan smem_plan(int K, int S, int M) {
     const int G = K / kGroup;
     const int gmax = (G + S - 1) / S;
     SmemPlan p;
-    p.x_off = (size_t)stages * kStageBytes;
+    p.x_off = (size_t)kStages * kStageBytes;
     p.x_row_bytes = (size_t)gmax * kGroup * 2 + 16;      // +16 B: rows land on other banks
     p.zero_off = p.x_off + (size_t)M * p.x_row_bytes;
     p.red_off = p.zero_off + 256;
     p.bar_off = p.red_off + (S > 1 ? (size_t)kWarps * 32 * 16 : 0);
-    p.total = p.bar_off + (size_t)(2 * kMaxStages + 1) * 8;
+    p.total = p.bar_off + (size_t)(2 * kStages + 1) * 8;
     return p;
 }
 
@@ -272,7 +271,7 @@ template <bool F32OUT, int MIN_BLOCKS>
 __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
 gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             const char *__restrict__ zp, const __nv_bfloat16 *__restrict__ x,
-            void *__restrict__ yv, uint32_t *err, int M, int K, int N, int S, int stages,
+            void *__restrict__ yv, uint32_t *err, int M, int K, int N, int S,
             uint32_t nib_mask, uint32_t bf16_magic) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int G = K / kGroup;
@@ -282,14 +281,14 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
     const int g1 = (int)((long long)(split + 1) * G / S);
     const int ng = g1 - g0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const SmemPlan plan = smem_plan(K, S, M, stages);
+    const SmemPlan plan = smem_plan(K, S, M);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + plan.bar_off);
-    uint64_t *empty = full + kMaxStages;
-    uint64_t *xbar = empty + kMaxStages;
+    uint64_t *empty = full + kStages;
+    uint64_t *xbar = empty + kStages;
     unsigned char *xs = smem + plan.x_off;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kWarps);
         }
@@ -309,34 +308,39 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             // The weights do not depend on the previous kernel in the stream:
             // request the first two groups before waiting for it, then x (which
             // the consumers need first), then the rest.
-            int issued = 0, slot = 0;
-            uint32_t phase = 0;                     // completed uses of `slot`, mod 2
+            int issued = 0;
+            uint32_t phase = 0;                     // round of the ring, mod 2
             const int first = ng < 2 ? ng : 2;
-            for (int s = 0; s < ng; ++s) {
-                if (s == first) {
-                    wait_prerequisites();
-                    mbar_expect_tx(xbar, (uint32_t)(M * ng * kGroup * 2));
-                    for (int m = 0; m < M; ++m)
-                        bulk_g2s(xs + m * plan.x_row_bytes,
-                                 x + (size_t)m * K + (size_t)g0 * kGroup,
-                                 (uint32_t)(ng * kGroup * 2), xbar);
+            for (int base = 0; base < ng && ok; base += kStages) {
+#pragma unroll
+                for (int i = 0; i < kStages; ++i) {
+                    const int s = base + i;
+                    if (s < ng && ok) {
+                        if (s == first) {
+                            wait_prerequisites();
+                            mbar_expect_tx(xbar, (uint32_t)(M * ng * kGroup * 2));
+                            for (int m = 0; m < M; ++m)
+                                bulk_g2s(xs + m * plan.x_row_bytes,
+                                         x + (size_t)m * K + (size_t)g0 * kGroup,
+                                         (uint32_t)(ng * kGroup * 2), xbar);
+                        }
+                        if (base > 0 && !mbar_wait(&empty[i], phase ^ 1u)) {
+                            ok = false;
+                        } else {
+                            unsigned char *st = smem + i * kStageBytes;
+                            const size_t rec = (size_t)b * G + g0 + s;
+                            mbar_expect_tx(&full[i], kStageBytes);
+                            bulk_g2s(st, qw + W4_HEADER_BYTES + rec * kRecWeights, kRecWeights,
+                                     &full[i]);
+                            bulk_g2s(st + kRecWeights, sc + rec * kRecScales, kRecScales,
+                                     &full[i]);
+                            bulk_g2s(st + kRecWeights + kRecScales, zp + rec * kRecZeros,
+                                     kRecZeros, &full[i]);
+                            ++issued;
+                        }
+                    }
                 }
-                if (s >= stages && !mbar_wait(&empty[slot], phase ^ 1u)) {
-                    ok = false;
-                    break;
-                }
-                unsigned char *st = smem + (size_t)slot * kStageBytes;
-                const size_t rec = (size_t)b * G + g0 + s;
-                mbar_expect_tx(&full[slot], kStageBytes);
-                bulk_g2s(st, qw + W4_HEADER_BYTES + rec * kRecWeights, kRecWeights, &full[slot]);
-                bulk_g2s(st + kRecWeights, sc + rec * kRecScales, kRecScales, &full[slot]);
-                bulk_g2s(st + kRecWeights + kRecScales, zp + rec * kRecZeros, kRecZeros,
-                         &full[slot]);
-                ++issued;
-                if (++slot == stages) {
-                    slot = 0;
-                    phase ^= 1u;
-                }
+                phase ^= 1u;
             }
             if (ng == first) {
                 wait_prerequisites();
@@ -347,8 +351,8 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             }
             if (!ok) {
                 // Give the copies already issued a bounded chance to land before exit.
-                for (int s = issued > stages ? issued - stages : 0; s < issued; ++s)
-                    mbar_wait(&full[s % stages], (s / stages) & 1);
+                for (int s = issued > kStages ? issued - kStages : 0; s < issued; ++s)
+                    mbar_wait(&full[s % kStages], (s / kStages) & 1);
                 atomicOr(err, 1u);
             }
         }
@@ -369,21 +373,23 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
                    : zpatch) + tq * 8;   // words 8tq .. 8tq+7 of each 32-word chunk
         const int xstride = has_x ? 64 : 0;     // words per group
         const float zq[4] = {0.f, 0.f, 0.f, 0.f};
-        int slot = 0;
-        uint32_t phase = 0;
-        for (int s = 0; s < ng && ok; ++s) {
-            if (!mbar_wait(&full[slot], phase)) {
-                ok = false;
-                break;
+        uint32_t phase = 0;                     // round of the ring, mod 2
+        for (int base = 0; base < ng && ok; base += kStages) {
+#pragma unroll
+            for (int i = 0; i < kStages; ++i) {
+                const int s = base + i;
+                if (s < ng && ok) {
+                    if (!mbar_wait(&full[i], phase)) {
+                        ok = false;
+                    } else {
+                        const GroupData g = read_group(smem + i * kStageBytes, warp, lane);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[i]);   // stage copied to registers
+                        group_mma(acc, g, xrow + s * xstride, zq, nib_mask, bf16_magic);
+                    }
+                }
             }
-            const GroupData g = read_group(smem + (size_t)slot * kStageBytes, warp, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);    // stage copied to registers
-            if (++slot == stages) {
-                slot = 0;
-                phase ^= 1u;
-            }
-            group_mma(acc, g, xrow + s * xstride, zq, nib_mask, bf16_magic);
+            phase ^= 1u;
         }
         if (!ok && lane == 0) atomicOr(err, 1u);
     }
@@ -428,7 +434,7 @@ bool gemv_shape(int K, int N, int num_sms, GemvShape *out) {
     long long best_cost = 0;
     for (int S : kCandidates) {
         if (S > G || S > kMaxSplits) continue;
-        if (smem_plan(K, S, W4_MAX_TOKENS, kMinStages).total > kBlockSmemBudget) continue;
+        if (smem_plan(K, S, W4_MAX_TOKENS).total > kBlockSmemBudget) continue;
         const long long ctas = (long long)NB * S;
         const long long waves = (ctas + slots - 1) / slots;
         const long long cost = waves * ((G + S - 1) / S + fill);
@@ -440,7 +446,7 @@ bool gemv_shape(int K, int N, int num_sms, GemvShape *out) {
     if (best_s == 0) return false;
     out->warps = kWarps;
     out->splits = best_s;
-    out->stages = kMinStages;
+    out->stages = kStages;
     return true;
 }
 
@@ -448,18 +454,10 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
                         const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
                         const GemvShape &shape, cudaStream_t stream) {
     const int S = shape.splits;
-    // The ring is as deep as the shared-memory budget allows for this M (the
-    // depth does not change the arithmetic, so results stay batch-invariant).
-    int stages = kMaxStages;
-    while (stages > kMinStages && smem_plan(K, S, M, stages).total > kBlockSmemBudget) --stages;
     // Small M: x is small, so three blocks fit per SM (more warps to hide
     // latency).  The split S, and so the arithmetic, is the same either way.
-    int stages3 = kMaxStages;
-    while (stages3 > kMinStages && smem_plan(K, S, M, stages3).total > kBlockSmemBudget3)
-        --stages3;
-    const bool three = M <= 2 && smem_plan(K, S, M, stages3).total <= kBlockSmemBudget3;
-    if (three) stages = stages3;
-    const SmemPlan plan = smem_plan(K, S, M, stages);
+    const SmemPlan plan = smem_plan(K, S, M);
+    const bool three = M <= 2 && plan.total <= kBlockSmemBudget3;
     static bool attr_done[2][2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -502,7 +500,7 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     return cudaLaunchKernelEx(&cfg, kern, q, static_cast<const char *>(scales),
                               static_cast<const char *>(zeros),
                               reinterpret_cast<const __nv_bfloat16 *>(x), y, err, M, K, N, S,
-                              stages, 0x000F000Fu, 0x43004300u);
+                              0x000F000Fu, 0x43004300u);
 }
 
 }  // namespace w4
