@@ -253,7 +253,7 @@ struct SmemPlan {
 };
 
 // Shared memory: [stages][weights | scales | zeros] [x rows as copied]
-// [256 zero bytes] [partials] [barriers]
+// [one zero row when M < 8] [partials] [barriers]
 __host__ __device__ inline SmemPlan smem_plan(int K, int S, int M) {
     const int G = K / kGroup;
     const int gmax = (G + S - 1) / S;
@@ -261,7 +261,7 @@ __host__ __device__ inline SmemPlan smem_plan(int K, int S, int M) {
     p.x_off = (size_t)kStages * kStageBytes;
     p.x_row_bytes = (size_t)gmax * kGroup * 2 + 16;      // +16 B: rows land on other banks
     p.zero_off = p.x_off + (size_t)M * p.x_row_bytes;
-    p.red_off = p.zero_off + 256;
+    p.red_off = p.zero_off + (M < W4_MAX_TOKENS ? p.x_row_bytes : 0);
     p.bar_off = p.red_off + (S > 1 ? (size_t)kWarps * 32 * 16 : 0);
     p.total = p.bar_off + (size_t)(2 * kStages + 1) * 8;
     return p;
@@ -359,38 +359,48 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
     } else {
         // ---- consumers: warp w owns tile 8b + w ----
         const int gq = lane >> 2, tq = lane & 3;
-        // Token columns >= M read a 256-byte zero patch at a fixed address.
-        uint32_t *zpatch = reinterpret_cast<uint32_t *>(smem + plan.zero_off);
-        if (threadIdx.x < 64) zpatch[threadIdx.x] = 0u;
+        // Token columns >= M read a row of zeros.
+        uint32_t *zrow = reinterpret_cast<uint32_t *>(smem + plan.zero_off);
+        if (M < W4_MAX_TOKENS)
+            for (int i = threadIdx.x; i < ng * 64; i += kWarps * 32) zrow[i] = 0u;
         consumer_sync();
         // x is used as copied: the kernel layout orders k inside each 64-k chunk
         // so that lane tq's eight B registers are the x pairs at
         // 64c + 16tq .. 64c + 16tq + 15 (see w4_repack.cu).
-        if (!mbar_wait(xbar, 0)) ok = false;
-        const bool has_x = gq < M;
         const uint32_t *xrow =
-            (has_x ? reinterpret_cast<const uint32_t *>(xs + (size_t)gq * plan.x_row_bytes)
-                   : zpatch) + tq * 8;   // words 8tq .. 8tq+7 of each 32-word chunk
-        const int xstride = has_x ? 64 : 0;     // words per group
+            (gq < M ? reinterpret_cast<const uint32_t *>(xs + (size_t)gq * plan.x_row_bytes)
+                    : zrow) + tq * 8;    // words 8tq .. 8tq+7 of each 32-word chunk
         const float zq[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t phase = 0;                     // round of the ring, mod 2
-        for (int base = 0; base < ng && ok; base += kStages) {
+        if (!mbar_wait(xbar, 0)) goto consumer_failed;
+        {
+            uint32_t phase = 0;                 // round of the ring, mod 2
+            int s = 0;
+            for (; s + kStages <= ng; s += kStages) {
 #pragma unroll
-            for (int i = 0; i < kStages; ++i) {
-                const int s = base + i;
-                if (s < ng && ok) {
-                    if (!mbar_wait(&full[i], phase)) {
-                        ok = false;
-                    } else {
-                        const GroupData g = read_group(smem + i * kStageBytes, warp, lane);
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&empty[i]);   // stage copied to registers
-                        group_mma(acc, g, xrow + s * xstride, zq, nib_mask, bf16_magic);
-                    }
+                for (int i = 0; i < kStages; ++i) {
+                    if (!mbar_wait(&full[i], phase)) goto consumer_failed;
+                    const GroupData g = read_group(smem + i * kStageBytes, warp, lane);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[i]);   // stage copied to registers
+                    group_mma(acc, g, xrow + (s + i) * 64, zq, nib_mask, bf16_magic);
+                }
+                phase ^= 1u;
+            }
+#pragma unroll
+            for (int i = 0; i < kStages - 1; ++i) {
+                if (s + i < ng) {
+                    if (!mbar_wait(&full[i], phase)) goto consumer_failed;
+                    const GroupData g = read_group(smem + i * kStageBytes, warp, lane);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[i]);
+                    group_mma(acc, g, xrow + (s + i) * 64, zq, nib_mask, bf16_magic);
                 }
             }
-            phase ^= 1u;
         }
+        goto consumer_done;
+    consumer_failed:
+        ok = false;
+    consumer_done:
         if (!ok && lane == 0) atomicOr(err, 1u);
     }
 
