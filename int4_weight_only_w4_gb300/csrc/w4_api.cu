@@ -38,7 +38,7 @@ w4_status gemv_common(const void *qweight, const void *scales, const void *zeros
     w4::GemvShape shape;
     if (!w4::gemv_shape(K, N, sms, &shape)) return W4_ERR_UNSUPPORTED;
     return cuda_status(w4::launch_gemv(qweight, scales, zeros, x, y, f32_out, M, K, N, shape,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+                                       sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace

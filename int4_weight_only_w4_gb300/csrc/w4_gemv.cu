@@ -371,6 +371,10 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             (gq < M ? reinterpret_cast<const uint32_t *>(xs + (size_t)gq * plan.x_row_bytes)
                     : zrow) + tq * 8;    // words 8tq .. 8tq+7 of each 32-word chunk
         const float zq[4] = {0.f, 0.f, 0.f, 0.f};
+        // Sleep (no polling) until the previous kernel in the stream is done:
+        // x may be its output, and a block launched early must not take issue
+        // slots from that kernel's still-running blocks.
+        wait_prerequisites();
         if (!mbar_wait(xbar, 0)) goto consumer_failed;
         {
             uint32_t phase = 0;                 // round of the ring, mod 2
@@ -462,7 +466,7 @@ bool gemv_shape(int K, int N, int num_sms, GemvShape *out) {
 
 cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zeros,
                         const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
-                        const GemvShape &shape, cudaStream_t stream) {
+                        const GemvShape &shape, int num_sms, cudaStream_t stream) {
     const int S = shape.splits;
     // Small M: x is small, so three blocks fit per SM (more warps to hide
     // latency).  The split S, and so the arithmetic, is the same either way.
@@ -485,10 +489,15 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = plan.total;
     cfg.stream = stream;
-    // Short (latency-bound) products overlap their start with the tail of the
-    // previous kernel in the stream (programmatic dependent launch); long ones
-    // measured faster without.
-    const bool overlap = (size_t)K * (size_t)N / 2 < kOverlapBelowBytes;
+    // Programmatic dependent launch (start while the previous kernel in the
+    // stream drains) pays off for short, latency-bound products and for grids
+    // of several waves.  A single-wave grid measured slower with it: its
+    // early-launched blocks take the free slot on every SM and the rest then
+    // pile onto fewer SMs.
+    const long long blocks = (long long)row_blocks(N) * S;
+    const int sms = num_sms > 0 ? num_sms : 1;
+    const bool overlap = (size_t)K * (size_t)N / 2 < kOverlapBelowBytes ||
+                         blocks > 3LL * sms;
     cudaLaunchAttribute attr[2];
     int na = 0;
     if (S > 1) {

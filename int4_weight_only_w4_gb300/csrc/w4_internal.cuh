@@ -67,6 +67,6 @@ bool gemv_shape(int K, int N, int num_sms, GemvShape *out);
 
 cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zeros,
                         const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
-                        const GemvShape &shape, cudaStream_t stream);
+                        const GemvShape &shape, int num_sms, cudaStream_t stream);
 
 }  // namespace w4
