@@ -156,6 +156,46 @@ w4_status w4_gemv_f32(const void *qweight, const void *scales, const void *zeros
                       w4_stream_t stream);
 
 /*
+ * Workspace for w4_gemv_ws on the current device, in bytes (depends on K, N
+ * and the SM count only).  Errors: W4_ERR_INVALID_ARG, W4_ERR_CUDA (no device).
+ */
+w4_status w4_gemv_workspace_bytes(int K, int N, size_t *bytes);
+
+/*
+ * The same product as w4_gemv, split evenly over one wave of thread blocks
+ * (three per SM): every block streams an equal contiguous run of the weight's
+ * 128-row x 128-k records, and the row blocks that fall between two blocks
+ * are combined through `workspace` by the last block to finish its part, in a
+ * fixed order (deterministic, no float atomics, no block ever waits for
+ * another).  It needs no thread-block clusters and never launches more than
+ * three blocks per SM, for callers that want that footprint; on the shapes
+ * measured on GB300, w4_gemv is faster.  Same result for a token whatever M
+ * is; bit-identical across calls.
+ *
+ *   qweight, scales, zeros, x, y : as for w4_gemv
+ *   workspace       : device, 256-byte aligned, at least
+ *                     w4_gemv_workspace_bytes(K, N) bytes, all zero before its
+ *                     first use.  It starts with one 32-bit counter per
+ *                     128-row block (padded to a multiple of 256 bytes), which
+ *                     every completed call leaves at zero again; the rest holds
+ *                     the partial sums of the last call.  So one workspace
+ *                     serves any number of calls in a row, but calls that
+ *                     share it must not overlap on the device; after a call
+ *                     that reported a kernel error, zero it again.
+ * Errors: W4_ERR_INVALID_ARG (also for a short or misaligned workspace),
+ * W4_ERR_UNSUPPORTED (M outside 1..8), W4_ERR_CUDA.
+ */
+w4_status w4_gemv_ws(const void *qweight, const void *scales, const void *zeros,
+                     const uint16_t *x, uint16_t *y, int M, int K, int N, void *workspace,
+                     size_t workspace_bytes, w4_stream_t stream);
+
+/* w4_gemv_ws writing the fp32 result before the bfloat16 cast (y: device
+ * float [M][N], 4-byte aligned).  For checking. */
+w4_status w4_gemv_ws_f32(const void *qweight, const void *scales, const void *zeros,
+                         const uint16_t *x, float *y, int M, int K, int N, void *workspace,
+                         size_t workspace_bytes, w4_stream_t stream);
+
+/*
  * The launch shape w4_gemv uses for an N x K weight on the current device:
  * 16-row tiles per thread block and the number of K splits (thread blocks of
  * one cluster that each reduce a slice of K and combine in a fixed order).

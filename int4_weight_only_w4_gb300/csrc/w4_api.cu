@@ -41,6 +41,22 @@ w4_status gemv_common(const void *qweight, const void *scales, const void *zeros
                                        sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+w4_status gemv_ws_common(const void *qweight, const void *scales, const void *zeros,
+                         const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
+                         void *workspace, size_t workspace_bytes, w4_stream_t stream) {
+    if (!qweight || !scales || !zeros || !x || !y || !workspace) return W4_ERR_INVALID_ARG;
+    if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
+    if (M < 1 || M > W4_MAX_TOKENS) return W4_ERR_UNSUPPORTED;
+    if (!aligned(qweight, 16) || !aligned(scales, 16) || !aligned(zeros, 16) ||
+        !aligned(x, 16) || !aligned(y, f32_out ? 4 : 2) || !aligned(workspace, 256))
+        return W4_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return W4_ERR_CUDA;
+    if (workspace_bytes < w4::gemv_ws_bytes(K, N, sms)) return W4_ERR_INVALID_ARG;
+    return cuda_status(w4::launch_gemv_ws(qweight, scales, zeros, x, y, f32_out, M, K, N,
+                                          workspace, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -121,6 +137,28 @@ w4_status w4_gemv(const void *qweight, const void *scales, const void *zeros, co
 w4_status w4_gemv_f32(const void *qweight, const void *scales, const void *zeros,
                       const uint16_t *x, float *y, int M, int K, int N, w4_stream_t stream) {
     return gemv_common(qweight, scales, zeros, x, y, true, M, K, N, stream);
+}
+
+w4_status w4_gemv_workspace_bytes(int K, int N, size_t *bytes) {
+    if (!valid_kn(K, N) || !bytes) return W4_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return W4_ERR_CUDA;
+    *bytes = w4::gemv_ws_bytes(K, N, sms);
+    return W4_OK;
+}
+
+w4_status w4_gemv_ws(const void *qweight, const void *scales, const void *zeros,
+                     const uint16_t *x, uint16_t *y, int M, int K, int N, void *workspace,
+                     size_t workspace_bytes, w4_stream_t stream) {
+    return gemv_ws_common(qweight, scales, zeros, x, y, false, M, K, N, workspace,
+                          workspace_bytes, stream);
+}
+
+w4_status w4_gemv_ws_f32(const void *qweight, const void *scales, const void *zeros,
+                         const uint16_t *x, float *y, int M, int K, int N, void *workspace,
+                         size_t workspace_bytes, w4_stream_t stream) {
+    return gemv_ws_common(qweight, scales, zeros, x, y, true, M, K, N, workspace,
+                          workspace_bytes, stream);
 }
 
 w4_status w4_gemv_config(int K, int N, int *tiles_per_block, int *k_splits) {

@@ -33,7 +33,7 @@ struct Header {
 };
 static_assert(sizeof(Header) == W4_HEADER_BYTES, "header size");
 
-inline int row_blocks(int N) { return (N + kBlockRows - 1) / kBlockRows; }
+__host__ __device__ inline int row_blocks(int N) { return (N + kBlockRows - 1) / kBlockRows; }
 constexpr size_t kErrorOffset = 28;   // byte offset of Header::kernel_error
 
 // Kernel-layout byte sizes (see w4_repack.cu for the layout itself).
@@ -68,5 +68,12 @@ bool gemv_shape(int K, int N, int num_sms, GemvShape *out);
 cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zeros,
                         const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
                         const GemvShape &shape, int num_sms, cudaStream_t stream);
+
+// Workspace path (w4_gemv_sk.cu): grid size, workspace bytes, launch.
+int gemv_ws_blocks(int K, int N, int num_sms);
+size_t gemv_ws_bytes(int K, int N, int num_sms);
+cudaError_t launch_gemv_ws(const void *qweight, const void *scales, const void *zeros,
+                           const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
+                           void *workspace, int num_sms, cudaStream_t stream);
 
 }  // namespace w4

@@ -49,6 +49,11 @@ _dequant = _decl("w4_dequant", _ST, _P, _P, _P, _I, _I, _P, _P)
 _gemv = _decl("w4_gemv", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_f32 = _decl("w4_gemv_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_config = _decl("w4_gemv_config", _ST, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I))
+_gemv_workspace_bytes = _decl("w4_gemv_workspace_bytes", _ST, _I, _I,
+                              ctypes.POINTER(ctypes.c_size_t))
+_gemv_ws = _decl("w4_gemv_ws", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P, ctypes.c_size_t, _P)
+_gemv_ws_f32 = _decl("w4_gemv_ws_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P, ctypes.c_size_t,
+                     _P)
 
 
 class Status(enum.IntEnum):
@@ -140,6 +145,42 @@ def gemv_f32(qweight, scales, zeros, x, y, M: int, K: int, N: int, stream=None) 
                   _stream(stream, x)), "w4_gemv_f32")
 
 
+def gemv_workspace_bytes(K: int, N: int) -> int:
+    """Bytes of workspace gemv_ws needs for N x K on the current device."""
+    n = ctypes.c_size_t()
+    _ok(_gemv_workspace_bytes(K, N, ctypes.byref(n)), "w4_gemv_workspace_bytes")
+    return n.value
+
+
+def workspace_counter_bytes(N: int) -> int:
+    """Bytes of the row-block counters at the start of a gemv_ws workspace."""
+    return ((N + 127) // 128 * 4 + 255) // 256 * 256
+
+
+def workspace(K: int, N: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace tensor for gemv_ws (allocated by torch)."""
+    return torch.zeros(gemv_workspace_bytes(K, N), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
+def gemv_ws(qweight, scales, zeros, x, y, M: int, K: int, N: int, workspace,
+            stream=None) -> None:
+    """w4_gemv_ws: as gemv, split evenly over one wave, combining through
+    `workspace` (zero-filled before first use; each call leaves its counters,
+    the first workspace_counter_bytes(N) bytes, at zero)."""
+    _ok(_gemv_ws(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, N,
+                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                 _stream(stream, x)), "w4_gemv_ws")
+
+
+def gemv_ws_f32(qweight, scales, zeros, x, y, M: int, K: int, N: int, workspace,
+                stream=None) -> None:
+    """w4_gemv_ws_f32: gemv_ws writing the fp32 result."""
+    _ok(_gemv_ws_f32(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, N,
+                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                     _stream(stream, x)), "w4_gemv_ws_f32")
+
+
 def gemv_config(K: int, N: int):
     """(16-row tiles per block, K splits) that w4_gemv uses for N x K."""
     t, s = _I(), _I()
@@ -156,19 +197,30 @@ class PackedWeight:
     scales: torch.Tensor    # uint8 bytes
     zeros: torch.Tensor     # uint8 bytes
 
-    def gemv(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-        """y = W x for x bfloat16 [M, K] on the device; returns y bfloat16 [M, N]."""
+    def gemv(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None,
+             workspace: torch.Tensor | None = None) -> torch.Tensor:
+        """y = W x for x bfloat16 [M, K] on the device; returns y bfloat16 [M, N].
+        With a workspace (see `workspace()`), uses gemv_ws."""
         M = x.shape[0]
         if y is None:
             y = torch.empty((M, self.N), dtype=torch.bfloat16, device=x.device)
-        gemv(self.qweight, self.scales, self.zeros, x, y, M, self.K, self.N, stream)
+        if workspace is None:
+            gemv(self.qweight, self.scales, self.zeros, x, y, M, self.K, self.N, stream)
+        else:
+            gemv_ws(self.qweight, self.scales, self.zeros, x, y, M, self.K, self.N, workspace,
+                    stream)
         return y
 
-    def gemv_f32(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None):
+    def gemv_f32(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None,
+                 workspace: torch.Tensor | None = None):
         M = x.shape[0]
         if y is None:
             y = torch.empty((M, self.N), dtype=torch.float32, device=x.device)
-        gemv_f32(self.qweight, self.scales, self.zeros, x, y, M, self.K, self.N, stream)
+        if workspace is None:
+            gemv_f32(self.qweight, self.scales, self.zeros, x, y, M, self.K, self.N, stream)
+        else:
+            gemv_ws_f32(self.qweight, self.scales, self.zeros, x, y, M, self.K, self.N,
+                        workspace, stream)
         return y
 
 

@@ -89,6 +89,17 @@ def test_gemv_argument_errors(lib, kw, want):
     assert gemv(lib, **kw) == want
 
 
+def test_gemv_ws_argument_errors(lib):
+    lib.w4_gemv_ws.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
+                               ctypes.c_size_t, P]
+    assert lib.w4_gemv_ws(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 16, None, 1 << 20, None) == 1
+    assert lib.w4_gemv_ws(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 128, 16, FAKE + 16, 1 << 20,
+                          None) == 1
+    assert lib.w4_gemv_ws(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 128, 16, FAKE, 1 << 20, None) == 2
+    lib.w4_gemv_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int, P]
+    assert lib.w4_gemv_workspace_bytes(100, 16, FAKE) == 1
+
+
 def test_dequant_and_repack_argument_errors(lib):
     lib.w4_dequant.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, P, P]
     assert lib.w4_dequant(None, FAKE, FAKE, 128, 4, FAKE, None) == 1

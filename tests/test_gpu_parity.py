@@ -19,14 +19,28 @@ def w4():
     return mod
 
 
-def run_gemv(w4, p, packed=None):
+PATHS = ["cluster", "ws"]     # w4_gemv (cluster split) and w4_gemv_ws (workspace split)
+
+
+def run_gemv(w4, p, packed=None, path="cluster"):
     qw, sc, zp, x = tu.to_device(p)
     if packed is None:
         packed = w4.pack(qw, sc, zp, p.K, p.N)
-    y32 = packed.gemv_f32(x)
-    y16 = packed.gemv(x)
+    ws = w4.workspace(p.K, p.N) if path == "ws" else None
+    y32 = packed.gemv_f32(x, workspace=ws)
+    y16 = packed.gemv(x, workspace=ws)
     torch.cuda.synchronize()
+    if ws is not None:
+        counters = ws[:w4.workspace_counter_bytes(p.N)]
+        assert int(counters.count_nonzero()) == 0, "workspace counters not left at zero"
     return y32.cpu().numpy(), tu.bf16_bits(y16), packed
+
+
+def path_splits(w4, path, K, N):
+    """Upper bound on the partial sums combined per output: the cluster split
+    uses gemv_config's count; the workspace split cuts a row at group
+    boundaries, so at most one piece per group."""
+    return w4.gemv_config(K, N)[1] if path == "cluster" else K // 128
 
 
 def oracle_rows(p, rows):
@@ -81,28 +95,30 @@ def test_dequant_extreme_scales(w4):
 CASES = [(name, M) for (name, K, N, Ms, _) in syn.SHAPES for M in Ms]
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("name,M", CASES)
-def test_gemv_workload_shapes(w4, name, M):
+def test_gemv_workload_shapes(w4, name, M, path):
     _, K, N, _, srange = syn.shape(name)
     p = syn.make_problem(f"{name}.M{M}", K, N, M, seed=0, scale_range=srange)
-    got32, got16, _ = run_gemv(w4, p)
-    _, splits = w4.gemv_config(K, N)
+    got32, got16, _ = run_gemv(w4, p, path=path)
+    splits = path_splits(w4, path, K, N)
     rows = sample_rows(N, np.random.default_rng(1)) if M * N * K > 2 ** 28 else np.arange(N)
     ref, refabs = oracle_rows(p, rows)
-    tu.check_gemv(got32[:, rows], got16[:, rows], ref, refabs, K, splits, f"{name} M={M}")
+    tu.check_gemv(got32[:, rows], got16[:, rows], ref, refabs, K, splits, f"{name} M={M} {path}")
 
 
 # ---- edge cases ---------------------------------------------------------------------
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("M,K,N", [(1, 128, 1), (3, 128, 17), (8, 256, 200), (2, 1152, 1000),
                                    (7, 384, 48), (4, 18944, 40), (5, 17408, 33),
-                                   (1, 640, 16), (6, 2048, 513)])
-def test_gemv_ragged_and_small(w4, M, K, N):
+                                   (1, 640, 16), (6, 2048, 513), (1, 4096, 20000)])
+def test_gemv_ragged_and_small(w4, M, K, N, path):
     p = syn.make_problem(f"edge.{M}.{K}.{N}", K, N, M, seed=2)
-    got32, got16, _ = run_gemv(w4, p)
+    got32, got16, _ = run_gemv(w4, p, path=path)
     ref, refabs = oracle.gemv_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N, with_abs=True)
-    _, splits = w4.gemv_config(K, N)
-    tu.check_gemv(got32, got16, ref, refabs, K, splits, f"edge {M},{K},{N}")
+    splits = path_splits(w4, path, K, N)
+    tu.check_gemv(got32, got16, ref, refabs, K, splits, f"edge {M},{K},{N} {path}")
 
 
 def test_split_paths_covered(w4):
@@ -110,7 +126,8 @@ def test_split_paths_covered(w4):
     assert 1 in splits and any(s > 1 for s in splits), splits
 
 
-def test_q_equals_z_gives_exact_zero(w4):
+@pytest.mark.parametrize("path", PATHS)
+def test_q_equals_z_gives_exact_zero(w4, path):
     M, K, N = 4, 1024, 100
     p = syn.make_problem("qz", K, N, M, seed=4)
     z = p.zeros
@@ -119,11 +136,12 @@ def test_q_equals_z_gives_exact_zero(w4):
     for j in range(8):
         words |= q[:, j::8] << np.uint32(4 * j)
     p.qweight = words
-    got32, got16, _ = run_gemv(w4, p)
+    got32, got16, _ = run_gemv(w4, p, path=path)
     assert np.all(got32 == 0.0) and np.all((got16 & 0x7FFF) == 0)
 
 
-def test_one_hot_and_identity_exact(w4):
+@pytest.mark.parametrize("path", PATHS)
+def test_one_hot_and_identity_exact(w4, path):
     M, K, N = 8, 512, 96
     p = syn.make_problem("onehot", K, N, M, seed=5)
     ks = [0, 1, 127, 128, 255, 300, 448, 511]
@@ -132,7 +150,7 @@ def test_one_hot_and_identity_exact(w4):
     for m in range(M):
         x[m, ks[m]] = vals[m]
     p.x = x
-    got32, _, _ = run_gemv(w4, p)
+    got32, _, _ = run_gemv(w4, p, path=path)
     ref = oracle.gemv_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N)
     assert np.array_equal(got32, ref.astype(np.float32))
     # identity pattern: q - z = 1 on the diagonal, 0 elsewhere; y = s * x exactly
@@ -146,52 +164,57 @@ def test_one_hot_and_identity_exact(w4):
         words |= q[:, j::8].astype(np.uint32) << np.uint32(4 * j)
     pi = syn.make_problem("ident", Kd, Nd, 3, seed=7)
     pi.qweight, pi.zeros = words, z.astype(np.uint8)
-    got32, _, _ = run_gemv(w4, pi)
+    got32, _, _ = run_gemv(w4, pi, path=path)
     ref = oracle.gemv_f64(pi.qweight, pi.scales, pi.zeros, pi.x, 3, Kd, Nd)
     assert np.array_equal(got32, ref.astype(np.float32))
 
 
-def test_linearity_power_of_two_exact(w4):
+@pytest.mark.parametrize("path", PATHS)
+def test_linearity_power_of_two_exact(w4, path):
     M, K, N = 3, 3584, 300
     p = syn.make_problem("lin", K, N, M, seed=8)
-    a32, _, packed = run_gemv(w4, p)
+    a32, _, packed = run_gemv(w4, p, path=path)
     xf = (p.x.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0)
     p2 = syn.Problem("lin2", M, K, N, p.qweight, p.scales, p.zeros,
                      (xf.view(np.uint32) >> 16).astype(np.uint16))
-    b32, _, _ = run_gemv(w4, p2, packed)
+    b32, _, _ = run_gemv(w4, p2, packed, path=path)
     assert np.array_equal(b32, 2 * a32)
 
 
-def test_determinism_and_batch_invariance(w4):
-    K, N = 18944, 3584
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("K,N", [(18944, 3584), (3584, 37888)])
+def test_determinism_and_batch_invariance(w4, path, K, N):
     p = syn.make_problem("det", K, N, 8, seed=9)
     qw, sc, zp, x = tu.to_device(p)
     packed = w4.pack(qw, sc, zp, K, N)
-    first = packed.gemv_f32(x).cpu()
+    ws = w4.workspace(K, N) if path == "ws" else None
+    first = packed.gemv_f32(x, workspace=ws).cpu()
     for _ in range(50):
-        assert torch.equal(packed.gemv_f32(x).cpu(), first)
+        assert torch.equal(packed.gemv_f32(x, workspace=ws).cpu(), first)
     for r in (0, 3, 7):
-        one = packed.gemv_f32(x[r:r + 1].contiguous()).cpu()
+        one = packed.gemv_f32(x[r:r + 1].contiguous(), workspace=ws).cpu()
         assert torch.equal(one[0], first[r])
-    five = packed.gemv_f32(x[:5].contiguous()).cpu()
+    five = packed.gemv_f32(x[:5].contiguous(), workspace=ws).cpu()
     assert torch.equal(five, first[:5])
 
 
-def test_graph_capture_replay(w4):
+@pytest.mark.parametrize("path", PATHS)
+def test_graph_capture_replay(w4, path):
     K, N, M = 3584, 4608, 1
     p = syn.make_problem("graph", K, N, M, seed=10)
     qw, sc, zp, x = tu.to_device(p)
     packed = w4.pack(qw, sc, zp, K, N)
-    y_eager = packed.gemv(x)
+    ws = w4.workspace(K, N) if path == "ws" else None
+    y_eager = packed.gemv(x, workspace=ws)
     y = torch.empty_like(y_eager)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        packed.gemv(x, y)            # warm-up on the capture stream
+        packed.gemv(x, y, workspace=ws)            # warm-up on the capture stream
     torch.cuda.current_stream().wait_stream(s)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        packed.gemv(x, y)
+        packed.gemv(x, y, workspace=ws)
     y.zero_()
     g.replay()
     torch.cuda.synchronize()
@@ -243,3 +266,20 @@ def test_argument_errors_on_device(w4):
     with pytest.raises(w4.W4Error) as e:
         w4.gemv(packed.qweight, packed.scales, packed.zeros, x, y, 2, 200, N)
     assert e.value.status == w4.Status.INVALID_ARG
+    short = torch.zeros(w4.gemv_workspace_bytes(K, N) - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(w4.W4Error) as e:
+        w4.gemv_ws(packed.qweight, packed.scales, packed.zeros, x, y, 2, K, N, short)
+    assert e.value.status == w4.Status.INVALID_ARG
+
+
+def test_ws_and_cluster_paths_agree(w4):
+    """Both splits compute the same sums in a different order: they differ by
+    no more than the sum of the two paths' fp32 rounding bounds."""
+    K, N, M = 3584, 37888, 2
+    p = syn.make_problem("paths", K, N, M, seed=14)
+    a32, _, packed = run_gemv(w4, p, path="cluster")
+    b32, _, _ = run_gemv(w4, p, packed, path="ws")
+    rows = sample_rows(N, np.random.default_rng(15))
+    _, refabs = oracle_rows(p, rows)
+    n = (8 + K // 128 + path_splits(w4, "cluster", K, N) + 1) + (8 + K // 128 + K // 128 + 1)
+    assert (np.abs(a32[:, rows].astype(np.float64) - b32[:, rows]) <= n * 2.0 ** -23 * refabs).all()
