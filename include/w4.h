@@ -52,7 +52,8 @@ typedef enum w4_status {
     W4_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, zero point > 15 */
     W4_ERR_UNSUPPORTED = 2,   /* M outside 1..8, or a call not allowed in stream capture */
     W4_ERR_LAYOUT = 3,        /* repacked buffer header does not match */
-    W4_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
+    W4_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    W4_ERR_SCRATCH_LIMIT = 5  /* needs more than W4_STATIC_SCRATCH_BYTES of scratch */
 } w4_status;
 
 #define W4_GROUP_SIZE 128
@@ -60,6 +61,8 @@ typedef enum w4_status {
 #define W4_LAYOUT_ID 1
 #define W4_LAYOUT_VERSION 3
 #define W4_HEADER_BYTES 128
+/* Size of the static device array behind w4_gemv_ws_static (4 MiB). */
+#define W4_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *w4_status_string(w4_status status);
@@ -194,6 +197,38 @@ w4_status w4_gemv_ws(const void *qweight, const void *scales, const void *zeros,
 w4_status w4_gemv_ws_f32(const void *qweight, const void *scales, const void *zeros,
                          const uint16_t *x, float *y, int M, int K, int N, void *workspace,
                          size_t workspace_bytes, w4_stream_t stream);
+
+/*
+ * w4_gemv_ws without a caller workspace: the scratch lives in a static device
+ * array of W4_STATIC_SCRATCH_BYTES inside the library, and this call allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).  The
+ * paper has no counterpart of this entry point; it is here for callers that
+ * cannot allocate device memory where they call the GEMV -- code running
+ * inside an allocator or memory-pool callback (an allocation there would
+ * re-enter the allocator), a plug-in of a host program that has reserved all
+ * device memory up front and hands out only the buffers it manages, or a
+ * latency-bound path that must not take the device-wide synchronisation and
+ * the failure mode of cudaMalloc.
+ *
+ *   qweight, scales, zeros, x, y, M, K, N, stream : as for w4_gemv
+ *
+ * The array costs W4_STATIC_SCRATCH_BYTES on every GPU that loads libw4,
+ * held until the process exits.  The first call on a device (the current one)
+ * looks up the array's device address; make that first call before any
+ * stream capture.  Every call on a device uses the same array, which keeps
+ * the last call's contents: each call clears the row-block counters it uses
+ * (an asynchronous memset on `stream`) and overwrites the partial sums before
+ * reading them, so consecutive calls are independent, but calls that overlap
+ * on the GPU (other streams, other host threads) race and give wrong results.
+ * A product needs w4_gemv_workspace_bytes(K, N) bytes of scratch; more than
+ * W4_STATIC_SCRATCH_BYTES is refused with W4_ERR_SCRATCH_LIMIT before
+ * anything else is checked or enqueued.
+ * Errors: W4_ERR_SCRATCH_LIMIT, W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED (M
+ * outside 1..8), W4_ERR_CUDA (no device, or the array could not be found).
+ */
+w4_status w4_gemv_ws_static(const void *qweight, const void *scales, const void *zeros,
+                            const uint16_t *x, uint16_t *y, int M, int K, int N,
+                            w4_stream_t stream);
 
 /*
  * The launch shape w4_gemv uses for an N x K weight on the current device:

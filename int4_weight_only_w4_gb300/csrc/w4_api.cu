@@ -68,6 +68,7 @@ const char *w4_status_string(w4_status status) {
         case W4_ERR_UNSUPPORTED: return "W4_ERR_UNSUPPORTED";
         case W4_ERR_LAYOUT: return "W4_ERR_LAYOUT";
         case W4_ERR_CUDA: return "W4_ERR_CUDA";
+        case W4_ERR_SCRATCH_LIMIT: return "W4_ERR_SCRATCH_LIMIT";
     }
     return "W4_ERR_UNKNOWN";
 }

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libw4.so")
 HEADER_BYTES = 128
 GROUP = 128
 MAX_TOKENS = 8
+STATIC_SCRATCH_BYTES = 4 * 1024 * 1024   # W4_STATIC_SCRATCH_BYTES
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -48,6 +49,7 @@ _check_header = _decl("w4_check_header", _ST, _P, _I, _I)
 _dequant = _decl("w4_dequant", _ST, _P, _P, _P, _I, _I, _P, _P)
 _gemv = _decl("w4_gemv", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_f32 = _decl("w4_gemv_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
+_gemv_ws_static = _decl("w4_gemv_ws_static", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_config = _decl("w4_gemv_config", _ST, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I))
 _gemv_workspace_bytes = _decl("w4_gemv_workspace_bytes", _ST, _I, _I,
                               ctypes.POINTER(ctypes.c_size_t))
@@ -62,6 +64,7 @@ class Status(enum.IntEnum):
     UNSUPPORTED = 2
     LAYOUT = 3
     CUDA = 4
+    SCRATCH_LIMIT = 5
 
 
 class W4Error(RuntimeError):
@@ -179,6 +182,14 @@ def gemv_ws_f32(qweight, scales, zeros, x, y, M: int, K: int, N: int, workspace,
     _ok(_gemv_ws_f32(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, N,
                      _ptr(workspace), workspace.numel() * workspace.element_size(),
                      _stream(stream, x)), "w4_gemv_ws_f32")
+
+
+def gemv_ws_static(qweight, scales, zeros, x, y, M: int, K: int, N: int, stream=None) -> None:
+    """w4_gemv_ws_static: gemv_ws with the library's static device scratch
+    (allocates nothing).  Calls on one device must not overlap on the GPU;
+    the first call on a device should come before any stream capture."""
+    _ok(_gemv_ws_static(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, N,
+                        _stream(stream, x)), "w4_gemv_ws_static")
 
 
 def gemv_config(K: int, N: int):

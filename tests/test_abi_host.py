@@ -44,7 +44,7 @@ def test_binding_names_match_abi():
 def test_status_strings(lib):
     lib.w4_status_string.restype = ctypes.c_char_p
     for code, name in enumerate(["W4_OK", "W4_ERR_INVALID_ARG", "W4_ERR_UNSUPPORTED",
-                                 "W4_ERR_LAYOUT", "W4_ERR_CUDA"]):
+                                 "W4_ERR_LAYOUT", "W4_ERR_CUDA", "W4_ERR_SCRATCH_LIMIT"]):
         assert lib.w4_status_string(code).decode() == name
     assert lib.w4_status_string(99).decode() == "W4_ERR_UNKNOWN"
 
