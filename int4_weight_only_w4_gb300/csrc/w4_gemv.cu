@@ -68,16 +68,53 @@ __host__ __device__ inline SmemPlan smem_plan(int K, int S, int M) {
     p.x_row_bytes = (size_t)gmax * kGroup * 2 + 16;      // +16 B: rows land on other banks
     p.zero_off = p.x_off + (size_t)M * p.x_row_bytes;
     p.red_off = p.zero_off + (M < W4_MAX_TOKENS ? p.x_row_bytes : 0);
-    p.bar_off = p.red_off + (S > 1 ? (size_t)kWarps * 32 * 16 : 0);
-    p.total = p.bar_off + (size_t)(2 * kStages + 1) * 8;
+    // Receive slots for the tiles this block reduces: ceil(8 / S) tiles, one
+    // 512-byte partial from each of the S blocks of the cluster.
+    p.bar_off = p.red_off + (S > 1 ? (size_t)S * ((kWarps + S - 1) / S) * 32 * 16 : 0);
+    p.total = p.bar_off + (size_t)(2 * kStages + 1) * 8 + 8;   // + the two constants
     return p;
+}
+
+// Combine the K slices of a cluster in rank order 0, 1, ..., S-1 (all
+// threads of every block of the cluster call this once, after their loop).
+// Tile w is reduced by block w % S: every block first stores its partial of
+// tile w into that block's receive slot (rank, w / S) through distributed
+// shared memory, then one cluster barrier (release / acquire) makes all
+// partials visible, and each reducing warp adds its S slots from its own
+// shared memory.  No block reads another block's memory after the barrier,
+// so none has to wait for the others before exiting.
+template <bool F32OUT>
+__device__ __forceinline__ void cluster_combine(float a0, float a1, float a2, float a3, void *yv,
+                                             unsigned char *red_bytes, int t, int S, int split,
+                                             int M, int N) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int J = (kWarps + S - 1) / S;                 // tiles reduced per block
+    float4 *red = reinterpret_cast<float4 *>(red_bytes);
+    cg::cluster_group cluster = cg::this_cluster();
+    if (warp < kWarps) {
+        float4 *dst = cluster.map_shared_rank(red, (unsigned)(warp % S));
+        dst[(split * J + warp / S) * 32 + lane] = make_float4(a0, a1, a2, a3);
+    }
+    cluster.sync();
+    if (warp < kWarps && (warp % S) == split) {
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        for (int r = 0; r < S; ++r) {
+            const float4 v = red[(r * J + warp / S) * 32 + lane];
+            s0 += v.x;
+            s1 += v.y;
+            s2 += v.z;
+            s3 += v.w;
+        }
+        const float tot[4] = {s0, s1, s2, s3};
+        store_tile<F32OUT>(yv, tot, t, lane, M, N);
+    }
 }
 
 template <bool F32OUT, int MIN_BLOCKS>
 __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
 gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             const char *__restrict__ zp, const __nv_bfloat16 *__restrict__ x,
-            void *__restrict__ yv, uint32_t *err, int M, int K, int N, int S,
+            void *__restrict__ yv, uint32_t *err, int M, int K, int N, int S, int pre,
             uint32_t nib_mask, uint32_t bf16_magic) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int G = K / kGroup;
@@ -100,6 +137,8 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
         }
         mbar_init(xbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        reinterpret_cast<uint32_t *>(xbar + 1)[0] = nib_mask;
+        reinterpret_cast<uint32_t *>(xbar + 1)[1] = bf16_magic;
     }
     __syncthreads();
 
@@ -112,24 +151,33 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
         // ---- producer ----
         if (lane == 0) {
             // The weights do not depend on the previous kernel in the stream:
-            // request the first two groups before waiting for it, then x (which
-            // the consumers need first), then the rest.
+            // under programmatic dependent launch, request the first `pre`
+            // groups before waiting for it; then x (which the consumers need
+            // first), then the rest.  Launched normally (pre = 0), the wait
+            // returns at once and x goes ahead of every weight copy.
             int issued = 0;
+            const int first = ng < pre ? ng : pre;  // < kStages: no ring waits needed
+            for (int s = 0; s < first; ++s) {
+                unsigned char *st = smem + s * kStageBytes;
+                const size_t rec = (size_t)b * G + g0 + s;
+                mbar_expect_tx(&full[s], kStageBytes);
+                bulk_g2s(st, qw + W4_HEADER_BYTES + rec * kRecWeights, kRecWeights, &full[s]);
+                bulk_g2s(st + kRecWeights, sc + rec * kRecScales, kRecScales, &full[s]);
+                bulk_g2s(st + kRecWeights + kRecScales, zp + rec * kRecZeros, kRecZeros,
+                         &full[s]);
+                ++issued;
+            }
+            wait_prerequisites();
+            mbar_expect_tx(xbar, (uint32_t)(M * ng * kGroup * 2));
+            for (int m = 0; m < M; ++m)
+                bulk_g2s(xs + m * plan.x_row_bytes, x + (size_t)m * K + (size_t)g0 * kGroup,
+                         (uint32_t)(ng * kGroup * 2), xbar);
             uint32_t phase = 0;                     // round of the ring, mod 2
-            const int first = ng < 2 ? ng : 2;
             for (int base = 0; base < ng && ok; base += kStages) {
 #pragma unroll
                 for (int i = 0; i < kStages; ++i) {
                     const int s = base + i;
-                    if (s < ng && ok) {
-                        if (s == first) {
-                            wait_prerequisites();
-                            mbar_expect_tx(xbar, (uint32_t)(M * ng * kGroup * 2));
-                            for (int m = 0; m < M; ++m)
-                                bulk_g2s(xs + m * plan.x_row_bytes,
-                                         x + (size_t)m * K + (size_t)g0 * kGroup,
-                                         (uint32_t)(ng * kGroup * 2), xbar);
-                        }
+                    if (s >= first && s < ng && ok) {
                         if (base > 0 && !mbar_wait(&empty[i], phase ^ 1u)) {
                             ok = false;
                         } else {
@@ -147,13 +195,6 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
                     }
                 }
                 phase ^= 1u;
-            }
-            if (ng == first) {
-                wait_prerequisites();
-                mbar_expect_tx(xbar, (uint32_t)(M * ng * kGroup * 2));
-                for (int m = 0; m < M; ++m)
-                    bulk_g2s(xs + m * plan.x_row_bytes, x + (size_t)m * K + (size_t)g0 * kGroup,
-                             (uint32_t)(ng * kGroup * 2), xbar);
             }
             if (!ok) {
                 // Give the copies already issued a bounded chance to land before exit.
@@ -177,6 +218,13 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             (gq < M ? reinterpret_cast<const uint32_t *>(xs + (size_t)gq * plan.x_row_bytes)
                     : zrow) + tq * 8;    // words 8tq .. 8tq+7 of each 32-word chunk
         const float zq[4] = {0.f, 0.f, 0.f, 0.f};
+        // The two conversion constants, read from shared memory so that they
+        // sit in ordinary registers: left as kernel parameters, the compiler
+        // may keep them in uniform registers, and a three-input logic
+        // operation takes only one of those, which costs a register move per
+        // extraction.
+        const uint32_t mask = reinterpret_cast<volatile uint32_t *>(xbar + 1)[0];
+        const uint32_t magic = reinterpret_cast<volatile uint32_t *>(xbar + 1)[1];
         // Sleep (no polling) until the previous kernel in the stream is done:
         // x may be its output, and a block launched early must not take issue
         // slots from that kernel's still-running blocks.
@@ -192,7 +240,7 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
                     const GroupData g = read_group(smem + i * kStageBytes, warp, lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[i]);   // stage copied to registers
-                    group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, nib_mask, bf16_magic);
+                    group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, mask, magic);
                 }
                 phase ^= 1u;
             }
@@ -203,7 +251,7 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
                     const GroupData g = read_group(smem + i * kStageBytes, warp, lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[i]);
-                    group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, nib_mask, bf16_magic);
+                    group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, mask, magic);
                 }
             }
         }
@@ -220,24 +268,8 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
         if (warp < kWarps && ok) store_tile<F32OUT>(yv, acc, t, lane, M, N);
         return;
     }
-    // Combine the K slices of the cluster in rank order 0, 1, ..., S-1.
-    float4 *red = reinterpret_cast<float4 *>(smem + plan.red_off);
-    if (warp < kWarps) red[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    if (warp < kWarps && (warp % S) == split) {
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-        for (int r = 0; r < S; ++r) {
-            const float4 v = *cluster.map_shared_rank(&red[warp * 32 + lane], r);
-            s0 += v.x;
-            s1 += v.y;
-            s2 += v.z;
-            s3 += v.w;
-        }
-        const float tot[4] = {s0, s1, s2, s3};
-        store_tile<F32OUT>(yv, tot, t, lane, M, N);
-    }
-    cluster.sync();
+    cluster_combine<F32OUT>(acc[0], acc[1], acc[2], acc[3], yv, smem + plan.red_off, t, S, split,
+                            M, N);
 }
 
 }  // namespace
@@ -325,7 +357,7 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     return cudaLaunchKernelEx(&cfg, kern, q, static_cast<const char *>(scales),
                               static_cast<const char *>(zeros),
                               reinterpret_cast<const __nv_bfloat16 *>(x), y, err, M, K, N, S,
-                              0x000F000Fu, 0x43004300u);
+                              overlap ? 2 : 0, 0x000F000Fu, 0x43004300u);
 }
 
 }  // namespace w4
