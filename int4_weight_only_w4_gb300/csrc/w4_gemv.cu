@@ -41,6 +41,10 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "w4_device.cuh"
 
 namespace cg = cooperative_groups;
@@ -302,6 +306,49 @@ bool gemv_shape(int K, int N, int num_sms, GemvShape *out) {
     return true;
 }
 
+namespace {
+
+struct DeviceSmem {
+    int per_sm = 0, reserved = 0, optin = 0;
+};
+
+// Shared memory per SM, reserved per block and the opt-in maximum per block
+// of device `dev`, read once.
+const DeviceSmem &device_smem(int dev) {
+    static DeviceSmem cache[64];
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    DeviceSmem &d = cache[dev];
+    if (d.per_sm == 0) {
+        cudaDeviceGetAttribute(&d.per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        cudaDeviceGetAttribute(&d.reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        cudaDeviceGetAttribute(&d.optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    }
+    return d;
+}
+
+// Clusters of this launch configuration that can be resident at once, cached.
+int active_clusters(const void *kern, cudaLaunchConfig_t cfg, int dev) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void *, size_t, unsigned, int>, int> cache;
+    const auto key = std::make_tuple(kern, cfg.dynamicSmemBytes, cfg.gridDim.y, dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = n;
+    return n;
+}
+
+}  // namespace
+
 cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zeros,
                         const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
                         const GemvShape &shape, int num_sms, cudaStream_t stream) {
@@ -314,11 +361,12 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const DeviceSmem &ds = device_smem(dev);
     auto kern = f32_out ? (three ? gemv_kernel<true, 3> : gemv_kernel<true, 2>)
                         : (three ? gemv_kernel<false, 3> : gemv_kernel<false, 2>);
-    if (dev < 64 && !attr_done[f32_out][three][dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(three ? kBlockSmemBudget3 : kBlockSmemBudget));
+    if (!attr_done[f32_out][three][dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ds.optin);
         if (e != cudaSuccess) return e;
         attr_done[f32_out][three][dev] = true;
     }
@@ -327,15 +375,6 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = plan.total;
     cfg.stream = stream;
-    // Programmatic dependent launch (start while the previous kernel in the
-    // stream drains) pays off for short, latency-bound products and for grids
-    // of several waves.  A single-wave grid measured slower with it: its
-    // early-launched blocks take the free slot on every SM and the rest then
-    // pile onto fewer SMs.
-    const long long blocks = (long long)row_blocks(N) * S;
-    const int sms = num_sms > 0 ? num_sms : 1;
-    const bool overlap = (size_t)K * (size_t)N / 2 < kOverlapBelowBytes ||
-                         blocks > 3LL * sms;
     cudaLaunchAttribute attr[2];
     int na = 0;
     if (S > 1) {
@@ -345,13 +384,45 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
         attr[na].val.clusterDim.z = 1;
         ++na;
     }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    // Residency.  A grid of one wave runs as long as its most loaded SM, so
+    // it should spread evenly: at most ceil(blocks / SMs) blocks per SM.
+    // Programmatic dependent launch starts blocks early in whatever slots
+    // the previous kernel leaves free; with room for three blocks per SM
+    // they stack up unevenly, so a grid that needs at most two per SM asks
+    // for enough shared memory that no more than that fit.  It then also
+    // overlaps its start with the previous kernel's end.  Grids that need
+    // three per SM launch without overlap (unless short); grids of several
+    // waves always overlap.
+    const long long blocks = (long long)row_blocks(N) * S;
+    const int sms = num_sms > 0 ? num_sms : 1;
+    const int need = blocks <= sms ? 1 : blocks <= 2LL * sms ? 2 : 3;
+    bool capped = false;
+    if (need < 3 && ds.per_sm > 0) {
+        const size_t pad = (size_t)(ds.per_sm / (need + 1) - ds.reserved + 16) / 16 * 16;
+        if (pad > plan.total && pad <= (size_t)ds.optin) {
+            cudaLaunchConfig_t padded = cfg;
+            padded.dynamicSmemBytes = pad;
+            // With clusters, only where the grid stays one wave with 10% of
+            // the cluster slots to spare: clusters are placed whole, within
+            // one GPC, and a grid that only just fits measured slower capped.
+            if (S == 1 ||
+                (long long)active_clusters((const void *)kern, padded, dev) * S * 10 >=
+                    blocks * 11) {
+                cfg.dynamicSmemBytes = pad;
+                capped = true;
+            }
+        }
+    }
+    const bool overlap = capped || (size_t)K * (size_t)N / 2 < kOverlapBelowBytes ||
+                         blocks > 3LL * sms;
     if (overlap) {
         attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
+        cfg.numAttrs = na;
     }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
     const char *q = static_cast<const char *>(qweight);
     uint32_t *err = reinterpret_cast<uint32_t *>(const_cast<char *>(q) + kErrorOffset);
     return cudaLaunchKernelEx(&cfg, kern, q, static_cast<const char *>(scales),
