@@ -292,7 +292,10 @@ bool gemv_shape(int K, int N, int num_sms, GemvShape *out) {
         if (S > G || S > kMaxSplits) continue;
         if (smem_plan(K, S, W4_MAX_TOKENS).total > kBlockSmemBudget) continue;
         const long long ctas = (long long)NB * S;
-        const long long waves = (ctas + slots - 1) / slots;
+        // A clustered grid counts as one wave only with 10% of the slots to
+        // spare, as in launch_gemv (beyond that it runs uncapped and slower).
+        const long long waves =
+            S == 1 ? (ctas + slots - 1) / slots : (ctas * 11 + slots * 10 - 1) / (slots * 10);
         const long long cost = waves * ((G + S - 1) / S + fill);
         if (best_s == 0 || cost <= best_cost) {
             best_s = S;
