@@ -232,12 +232,17 @@ w4_status w4_gemv_ws_static(const void *qweight, const void *scales, const void 
 
 /*
  * The launch shape w4_gemv uses for an N x K weight on the current device:
- * 16-row tiles per thread block and the number of K splits (thread blocks of
- * one cluster that each reduce a slice of K and combine in a fixed order).
- * Depends on K and N only, never on M.  Outputs may be NULL.
+ * 16-row tiles per thread block, the number of K splits (thread blocks of
+ * one cluster that each reduce a slice of K and combine in a fixed order),
+ * and whether the zero point is folded out of the inner product (1: each
+ * group computes sum (128 + q) x - (128 + z) sum x in fp32, chosen when a
+ * block streams at least 8 groups; 0: the tensor-core operand is q - z,
+ * exactly).  Both are the same sum up to fp32 rounding.  Depends on K and N
+ * only, never on M.  Outputs may be NULL.
  * Errors: W4_ERR_INVALID_ARG, W4_ERR_CUDA (no device).
  */
-w4_status w4_gemv_config(int K, int N, int *tiles_per_block, int *k_splits);
+w4_status w4_gemv_config(int K, int N, int *tiles_per_block, int *k_splits,
+                         int *zero_point_folded);
 
 #ifdef __cplusplus
 }

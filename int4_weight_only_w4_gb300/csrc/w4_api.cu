@@ -162,7 +162,8 @@ w4_status w4_gemv_ws_f32(const void *qweight, const void *scales, const void *ze
                           workspace_bytes, stream);
 }
 
-w4_status w4_gemv_config(int K, int N, int *tiles_per_block, int *k_splits) {
+w4_status w4_gemv_config(int K, int N, int *tiles_per_block, int *k_splits,
+                         int *zero_point_folded) {
     if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
     const int sms = device_sms();
     if (sms <= 0) return W4_ERR_CUDA;
@@ -170,6 +171,7 @@ w4_status w4_gemv_config(int K, int N, int *tiles_per_block, int *k_splits) {
     if (!w4::gemv_shape(K, N, sms, &shape)) return W4_ERR_UNSUPPORTED;
     if (tiles_per_block) *tiles_per_block = shape.warps;
     if (k_splits) *k_splits = shape.splits;
+    if (zero_point_folded) *zero_point_folded = shape.fold ? 1 : 0;
     return W4_OK;
 }
 

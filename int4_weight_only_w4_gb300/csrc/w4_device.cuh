@@ -126,7 +126,9 @@ __device__ __forceinline__ void consumer_sync() {
 // ncl, nch = -(128 + z) for rows gq and gq + 8 as bf16 pairs.  mask and magic
 // are 0x000F000F and 0x43004300, passed in registers so that each extraction
 // is one three-input logic operation.  FIRST: the accumulators start from zero.
-template <bool FIRST>
+// SUBZ: subtract 128 + z from every A register (A = q - z exactly); without
+// it A = 128 + q and the caller removes (128 + z) * sum(x) per group.
+template <bool FIRST, bool SUBZ = true>
 __device__ __forceinline__ void chunk_mma(float (&d)[2][4], const uint4 &w, const uint4 &bl,
                                           const uint4 &bh, uint32_t ncl, uint32_t nch,
                                           const float (&zq)[4], uint32_t mask, uint32_t magic) {
@@ -139,10 +141,12 @@ __device__ __forceinline__ void chunk_mma(float (&d)[2][4], const uint4 &w, cons
         uint32_t a1 = and_or(wd >> 4, mask, magic);
         uint32_t a2 = and_or(wd >> 8, mask, magic);
         uint32_t a3 = and_or(wd >> 12, mask, magic);
-        a0 = bf16x2_add(a0, ncl);
-        a1 = bf16x2_add(a1, nch);
-        a2 = bf16x2_add(a2, ncl);
-        a3 = bf16x2_add(a3, nch);
+        if (SUBZ) {
+            a0 = bf16x2_add(a0, ncl);
+            a1 = bf16x2_add(a1, nch);
+            a2 = bf16x2_add(a2, ncl);
+            a3 = bf16x2_add(a3, nch);
+        }
         if (FIRST && (j & 1) == 0)
             mma_bf16_16816_first(d[j >> 1], a0, a1, a2, a3, b[2 * j], b[2 * j + 1], zq);
         else
@@ -199,6 +203,30 @@ __device__ __forceinline__ void group_mma(float (&acc)[4], const GroupData &g, c
     acc[1] = fmaf(d[0][1] + d[1][1], sl, acc[1]);
     acc[2] = fmaf(d[0][2] + d[1][2], sh, acc[2]);
     acc[3] = fmaf(d[0][3] + d[1][3], sh, acc[3]);
+}
+
+// group_mma with the zero point folded out of the inner product:
+//   sum_k (q - z) x = sum_k (128 + q) x - (128 + z) * sum_k x,
+// so the A registers are the extracted 128 + q as they are (no per-register
+// subtraction) and each of the lane's four outputs takes one fp32 fma with
+// xs = (sum of the group's x for token 2tq, for token 2tq + 1).  The
+// product (128 + z) * sum_k x is exact inside the fma.
+__device__ __forceinline__ void group_mma_folded(float (&acc)[4], const GroupData &g,
+                                                 const GroupB &b, float2 xs,
+                                                 const float (&zq)[4], uint32_t mask,
+                                                 uint32_t magic) {
+    // -(128 + z) in fp32: 0xC3000000 is -128, and z << 16 adds z to it.
+    const float nzl = __uint_as_float(0xC3000000u | ((g.zb & 0xFu) << 16));
+    const float nzh = __uint_as_float(0xC3000000u | ((g.zb >> 4) << 16));
+    const float sl = __half2float(__ushort_as_half((unsigned short)(g.sp & 0xFFFFu)));
+    const float sh = __half2float(__ushort_as_half((unsigned short)(g.sp >> 16)));
+    float d[2][4];
+    chunk_mma<true, false>(d, g.w0, b.b0l, b.b0h, 0u, 0u, zq, mask, magic);
+    chunk_mma<false, false>(d, g.w1, b.b1l, b.b1h, 0u, 0u, zq, mask, magic);
+    acc[0] = fmaf(fmaf(nzl, xs.x, d[0][0] + d[1][0]), sl, acc[0]);
+    acc[1] = fmaf(fmaf(nzl, xs.y, d[0][1] + d[1][1]), sl, acc[1]);
+    acc[2] = fmaf(fmaf(nzh, xs.x, d[0][2] + d[1][2]), sh, acc[2]);
+    acc[3] = fmaf(fmaf(nzh, xs.y, d[0][3] + d[1][3]), sh, acc[3]);
 }
 
 template <bool F32OUT>

@@ -56,14 +56,15 @@ constexpr int kStageBytes = kRecWeights + kRecScales + kRecZeros;   // 8512
 constexpr int kStages = 6;                          // shared-memory ring depth
 constexpr size_t kBlockSmemBudget = 113 * 1024;     // two blocks per SM
 constexpr size_t kBlockSmemBudget3 = 74 * 1024;     // three blocks per SM (small M)
+constexpr int kFoldMinGroups = 8;                   // see gemv_shape
 constexpr size_t kOverlapBelowBytes = 16u << 20;    // packed weights of a "short" product
 
 struct SmemPlan {
-    size_t x_off, x_row_bytes, zero_off, red_off, bar_off, total;
+    size_t x_off, x_row_bytes, zero_off, red_off, xsum_off, bar_off, total;
 };
 
 // Shared memory: [stages][weights | scales | zeros] [x rows as copied]
-// [one zero row when M < 8] [partials] [barriers]
+// [one zero row when M < 8] [partials] [per-group sums of x] [barriers]
 __host__ __device__ inline SmemPlan smem_plan(int K, int S, int M) {
     const int G = K / kGroup;
     const int gmax = (G + S - 1) / S;
@@ -74,7 +75,8 @@ __host__ __device__ inline SmemPlan smem_plan(int K, int S, int M) {
     p.red_off = p.zero_off + (M < W4_MAX_TOKENS ? p.x_row_bytes : 0);
     // Receive slots for the tiles this block reduces: ceil(8 / S) tiles, one
     // 512-byte partial from each of the S blocks of the cluster.
-    p.bar_off = p.red_off + (S > 1 ? (size_t)S * ((kWarps + S - 1) / S) * 32 * 16 : 0);
+    p.xsum_off = p.red_off + (S > 1 ? (size_t)S * ((kWarps + S - 1) / S) * 32 * 16 : 0);
+    p.bar_off = p.xsum_off + (size_t)gmax * W4_MAX_TOKENS * 4;   // float [gmax][8]
     p.total = p.bar_off + (size_t)(2 * kStages + 1) * 8 + 8;   // + the two constants
     return p;
 }
@@ -114,7 +116,7 @@ __device__ __forceinline__ void cluster_combine(float a0, float a1, float a2, fl
     }
 }
 
-template <bool F32OUT, int MIN_BLOCKS>
+template <bool F32OUT, int MIN_BLOCKS, bool FOLD>
 __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
 gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             const char *__restrict__ zp, const __nv_bfloat16 *__restrict__ x,
@@ -212,8 +214,12 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
         const int gq = lane >> 2, tq = lane & 3;
         // Token columns >= M read a row of zeros.
         uint32_t *zrow = reinterpret_cast<uint32_t *>(smem + plan.zero_off);
-        if (M < W4_MAX_TOKENS)
+        float *xsum = reinterpret_cast<float *>(smem + plan.xsum_off);
+        if (M < W4_MAX_TOKENS) {
             for (int i = threadIdx.x; i < ng * 64; i += kWarps * 32) zrow[i] = 0u;
+            for (int i = threadIdx.x; i < ng * W4_MAX_TOKENS; i += kWarps * 32)
+                if ((i & (W4_MAX_TOKENS - 1)) >= M) xsum[i] = 0.f;
+        }
         consumer_sync();
         // x is used as copied: the kernel layout orders k inside each 64-k chunk
         // so that lane tq's eight B registers are the x pairs at
@@ -233,8 +239,73 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
         // x may be its output, and a block launched early must not take issue
         // slots from that kernel's still-running blocks.
         wait_prerequisites();
-        if (!mbar_wait(xbar, 0)) goto consumer_failed;
         {
+            // Per group and token, the sum of the group's 128 x values, for the
+            // zero-point term of group_mma_folded.  The fp32 arithmetic is
+            // fixed: eight partial sums of 16 consecutive values (left to
+            // right), then the pairwise tree ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)).
+            // Only the assignment of that work to threads depends on the
+            // number of (group, token) pairs: tpp threads per pair, each with
+            // 8 / tpp partials, joined by shuffles that follow the same tree.
+            // Every consumer thread takes part in the barrier below even if
+            // its wait gave up.
+            const bool x_ok = mbar_wait(xbar, 0);
+            if (FOLD && x_ok) {
+                const int pairs = ng * M;
+                int tpp = 8;
+                while (tpp > 1 && pairs * tpp > kWarps * 32) tpp >>= 1;
+                const int per = 8 / tpp;
+                for (int base = 0; base < pairs * tpp; base += kWarps * 32) {
+                    const int idx = base + (int)threadIdx.x;
+                    const int pair = idx / tpp, sub = idx - pair * tpp;
+                    float part[8];
+                    if (pair < pairs) {
+                        const int gl = pair / M, m = pair - gl * M;
+                        const uint4 *src = reinterpret_cast<const uint4 *>(
+                            xs + (size_t)m * plan.x_row_bytes + (size_t)gl * kGroup * 2 +
+                            (size_t)sub * per * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            if (j < per) {
+                                const uint4 u0 = src[2 * j], u1 = src[2 * j + 1];
+                                const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w,
+                                                       u1.x, u1.y, u1.z, u1.w};
+                                float acc_j = __uint_as_float(w[0] << 16);
+#pragma unroll
+                                for (int e = 1; e < 16; ++e)
+                                    acc_j += __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u)
+                                                                     : (w[e >> 1] << 16));
+                                part[j] = acc_j;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) part[j] = 0.f;
+                    }
+                    // this thread's subtree over its `per` partials
+                    if (per >= 2) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (2 * j + 1 < per) part[2 * j] = part[2 * j] + part[2 * j + 1];
+                    }
+                    if (per >= 4) {
+                        part[0] = part[0] + part[2];
+                        if (per == 8) part[4] = part[4] + part[6];
+                    }
+                    if (per == 8) part[0] = part[0] + part[4];
+                    float v = part[0];
+                    for (int o = 1; o < tpp; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+                    if (sub == 0 && pair < pairs) {
+                        const int gl = pair / M, m = pair - gl * M;
+                        xsum[gl * W4_MAX_TOKENS + m] = v;
+                    }
+                }
+            }
+            if constexpr (FOLD) consumer_sync();
+            if (!x_ok) goto consumer_failed;
+        }
+        {
+            const float2 *xs2 = reinterpret_cast<const float2 *>(xsum) + tq;
             uint32_t phase = 0;                 // round of the ring, mod 2
             int s = 0;
             for (; s + kStages <= ng; s += kStages) {
@@ -244,7 +315,11 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
                     const GroupData g = read_group(smem + i * kStageBytes, warp, lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[i]);   // stage copied to registers
-                    group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, mask, magic);
+                    if constexpr (FOLD)
+                        group_mma_folded(acc, g, load_b(xrow + (s + i) * 64), xs2[(s + i) * 4],
+                                         zq, mask, magic);
+                    else
+                        group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, mask, magic);
                 }
                 phase ^= 1u;
             }
@@ -255,7 +330,11 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
                     const GroupData g = read_group(smem + i * kStageBytes, warp, lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[i]);
-                    group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, mask, magic);
+                    if constexpr (FOLD)
+                        group_mma_folded(acc, g, load_b(xrow + (s + i) * 64), xs2[(s + i) * 4],
+                                         zq, mask, magic);
+                    else
+                        group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, mask, magic);
                 }
             }
         }
@@ -306,6 +385,10 @@ bool gemv_shape(int K, int N, int num_sms, GemvShape *out) {
     out->warps = kWarps;
     out->splits = best_s;
     out->stages = kStages;
+    // Fold the zero point out of the inner product when a block streams at
+    // least kFoldMinGroups groups: it saves the per-weight subtraction but
+    // adds a prologue (the group sums of x) that short blocks cannot hide.
+    out->fold = (G + best_s - 1) / best_s >= kFoldMinGroups;
     return true;
 }
 
@@ -360,18 +443,24 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     // latency).  The split S, and so the arithmetic, is the same either way.
     const SmemPlan plan = smem_plan(K, S, M);
     const bool three = M <= 2 && plan.total <= kBlockSmemBudget3;
-    static bool attr_done[2][2][64] = {};
+    static bool attr_done[2][2][2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const DeviceSmem &ds = device_smem(dev);
-    auto kern = f32_out ? (three ? gemv_kernel<true, 3> : gemv_kernel<true, 2>)
-                        : (three ? gemv_kernel<false, 3> : gemv_kernel<false, 2>);
-    if (!attr_done[f32_out][three][dev]) {
+    using Kern = void (*)(const char *, const char *, const char *, const __nv_bfloat16 *,
+                          void *, uint32_t *, int, int, int, int, int, uint32_t, uint32_t);
+    static const Kern kKernels[2][2][2] = {
+        {{gemv_kernel<false, 2, false>, gemv_kernel<false, 2, true>},
+         {gemv_kernel<false, 3, false>, gemv_kernel<false, 3, true>}},
+        {{gemv_kernel<true, 2, false>, gemv_kernel<true, 2, true>},
+         {gemv_kernel<true, 3, false>, gemv_kernel<true, 3, true>}}};
+    const Kern kern = kKernels[f32_out][three][shape.fold];
+    if (!attr_done[f32_out][three][shape.fold][dev]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ds.optin);
         if (e != cudaSuccess) return e;
-        attr_done[f32_out][three][dev] = true;
+        attr_done[f32_out][three][shape.fold][dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)row_blocks(N), (unsigned)S, 1);

@@ -59,6 +59,7 @@ struct GemvShape {
     int warps;    // consumer warps per block; each owns one 16-row tile
     int splits;   // K splits = blocks per cluster
     int stages;   // depth of the shared-memory weight ring
+    bool fold;    // zero point folded out of the inner product (see w4_gemv.cu)
 };
 
 // Launch shape for an N x K weight (independent of M).  Returns false if no

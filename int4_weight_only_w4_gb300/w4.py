@@ -50,7 +50,8 @@ _dequant = _decl("w4_dequant", _ST, _P, _P, _P, _I, _I, _P, _P)
 _gemv = _decl("w4_gemv", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_f32 = _decl("w4_gemv_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_ws_static = _decl("w4_gemv_ws_static", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
-_gemv_config = _decl("w4_gemv_config", _ST, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I))
+_gemv_config = _decl("w4_gemv_config", _ST, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
+                     ctypes.POINTER(_I))
 _gemv_workspace_bytes = _decl("w4_gemv_workspace_bytes", _ST, _I, _I,
                               ctypes.POINTER(ctypes.c_size_t))
 _gemv_ws = _decl("w4_gemv_ws", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P, ctypes.c_size_t, _P)
@@ -193,10 +194,11 @@ def gemv_ws_static(qweight, scales, zeros, x, y, M: int, K: int, N: int, stream=
 
 
 def gemv_config(K: int, N: int):
-    """(16-row tiles per block, K splits) that w4_gemv uses for N x K."""
-    t, s = _I(), _I()
-    _ok(_gemv_config(K, N, ctypes.byref(t), ctypes.byref(s)), "w4_gemv_config")
-    return t.value, s.value
+    """(16-row tiles per block, K splits, zero point folded) that w4_gemv uses
+    for N x K."""
+    t, s, f = _I(), _I(), _I()
+    _ok(_gemv_config(K, N, ctypes.byref(t), ctypes.byref(s), ctypes.byref(f)), "w4_gemv_config")
+    return t.value, s.value, bool(f.value)
 
 
 @dataclass

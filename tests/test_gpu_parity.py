@@ -1,6 +1,10 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
 same seeded inputs.  Dequantisation must be bit-exact; the GEMV must meet the
-tolerances in w4_testutil; closed-form cases must be exact."""
+tolerances in w4_testutil.  Closed-form cases are exact where the arithmetic
+makes them so (one-hot x and power-of-two scaling on both splits; q = z and the
+identity pattern on the workspace split, whose tensor-core operand is q - z
+exactly) and within the derived fp32 bound otherwise (the cluster split folds
+the zero point out of the inner product)."""
 import numpy as np
 import pytest
 
@@ -41,6 +45,18 @@ def path_splits(w4, path, K, N):
     uses gemv_config's count; the workspace split cuts a row at group
     boundaries, so at most one piece per group."""
     return w4.gemv_config(K, N)[1] if path == "cluster" else K // 128
+
+
+def folds(w4, path, K, N):
+    """Whether the path folds the zero point out of the inner product."""
+    return path == "cluster" and w4.gemv_config(K, N)[2]
+
+
+def bound_terms(w4, path, p, rows, refabs):
+    """(magnitudes, extra rounding steps) of the fp32 bound for a path."""
+    if folds(w4, path, p.K, p.N):
+        return tu.folded_abs(p, rows), tu.FOLD_EXTRA_STEPS
+    return refabs, 0
 
 
 def oracle_rows(p, rows):
@@ -104,7 +120,9 @@ def test_gemv_workload_shapes(w4, name, M, path):
     splits = path_splits(w4, path, K, N)
     rows = sample_rows(N, np.random.default_rng(1)) if M * N * K > 2 ** 28 else np.arange(N)
     ref, refabs = oracle_rows(p, rows)
-    tu.check_gemv(got32[:, rows], got16[:, rows], ref, refabs, K, splits, f"{name} M={M} {path}")
+    mag, extra = bound_terms(w4, path, p, rows, refabs)
+    tu.check_gemv(got32[:, rows], got16[:, rows], ref, mag, K, splits, f"{name} M={M} {path}",
+                  extra)
 
 
 # ---- edge cases ---------------------------------------------------------------------
@@ -118,17 +136,24 @@ def test_gemv_ragged_and_small(w4, M, K, N, path):
     got32, got16, _ = run_gemv(w4, p, path=path)
     ref, refabs = oracle.gemv_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N, with_abs=True)
     splits = path_splits(w4, path, K, N)
-    tu.check_gemv(got32, got16, ref, refabs, K, splits, f"edge {M},{K},{N} {path}")
+    mag, extra = bound_terms(w4, path, p, None, refabs)
+    tu.check_gemv(got32, got16, ref, mag, K, splits, f"edge {M},{K},{N} {path}", extra)
 
 
 def test_split_paths_covered(w4):
-    splits = {w4.gemv_config(K, N)[1] for (_, K, N, _, _) in syn.SHAPES}
+    cfg = [w4.gemv_config(K, N) for (_, K, N, _, _) in syn.SHAPES]
+    splits = {c[1] for c in cfg}
     assert 1 in splits and any(s > 1 for s in splits), splits
+    assert {c[2] for c in cfg} == {False, True}, cfg
 
 
 @pytest.mark.parametrize("path", PATHS)
-def test_q_equals_z_gives_exact_zero(w4, path):
-    M, K, N = 4, 1024, 100
+@pytest.mark.parametrize("K", [1024, 8192])
+def test_q_equals_z_gives_zero(w4, path, K):
+    """q = z everywhere: y = 0, exactly where the tensor-core operand is q - z,
+    within the fp32 bound of (128 + z) sum x - (128 + z) sum x where the zero
+    point is folded (the cluster split at K = 8192)."""
+    M, N = 4, 100
     p = syn.make_problem("qz", K, N, M, seed=4)
     z = p.zeros
     q = np.repeat(z, 128, axis=1).astype(np.uint32)
@@ -137,14 +162,28 @@ def test_q_equals_z_gives_exact_zero(w4, path):
         words |= q[:, j::8] << np.uint32(4 * j)
     p.qweight = words
     got32, got16, _ = run_gemv(w4, p, path=path)
-    assert np.all(got32 == 0.0) and np.all((got16 & 0x7FFF) == 0)
+    if not folds(w4, path, K, N):
+        assert np.all(got32 == 0.0) and np.all((got16 & 0x7FFF) == 0)
+    else:
+        n = 8 + K // 128 + path_splits(w4, path, K, N) + 1 + tu.FOLD_EXTRA_STEPS
+        assert (np.abs(got32) <= n * 2.0 ** -23 * tu.folded_abs(p)).all()
+        assert np.array_equal(got16, oracle.bf16_rne(got32))
 
 
 @pytest.mark.parametrize("path", PATHS)
-def test_one_hot_and_identity_exact(w4, path):
+@pytest.mark.parametrize("Kd", [256, 8192])
+def test_one_hot_and_identity(w4, path, Kd):
+    """One-hot x: exact on both splits and both arithmetics (a single nonzero
+    product per output).  Identity pattern (q - z = 1 on the diagonal): exact
+    where the operand is q - z, within the fp32 bound where the zero point is
+    folded."""
     M, K, N = 8, 512, 96
+    if Kd == 8192:
+        K = 8192
+        ks = [0, 1, 127, 128, 2000, 4095, 6000, 8191]
+    else:
+        ks = [0, 1, 127, 128, 255, 300, 448, 511]
     p = syn.make_problem("onehot", K, N, M, seed=5)
-    ks = [0, 1, 127, 128, 255, 300, 448, 511]
     x = np.zeros((M, K), np.uint16)
     vals = [0x3F80, 0xC040, 0x3E20, 0x4109, 0xBF00, 0x3F81, 0x4000, 0xC2F6]
     for m in range(M):
@@ -154,7 +193,7 @@ def test_one_hot_and_identity_exact(w4, path):
     ref = oracle.gemv_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N)
     assert np.array_equal(got32, ref.astype(np.float32))
     # identity pattern: q - z = 1 on the diagonal, 0 elsewhere; y = s * x exactly
-    Kd = Nd = 256
+    Nd = 256
     z = np.random.default_rng(6).integers(0, 15, size=(Nd, Kd // 128))
     q = np.repeat(z, 128, axis=1)
     for n in range(Nd):
@@ -166,7 +205,11 @@ def test_one_hot_and_identity_exact(w4, path):
     pi.qweight, pi.zeros = words, z.astype(np.uint8)
     got32, _, _ = run_gemv(w4, pi, path=path)
     ref = oracle.gemv_f64(pi.qweight, pi.scales, pi.zeros, pi.x, 3, Kd, Nd)
-    assert np.array_equal(got32, ref.astype(np.float32))
+    if not folds(w4, path, Kd, Nd):
+        assert np.array_equal(got32, ref.astype(np.float32))
+    else:
+        n = 8 + Kd // 128 + path_splits(w4, path, Kd, Nd) + 1 + tu.FOLD_EXTRA_STEPS
+        assert (np.abs(got32 - ref) <= n * 2.0 ** -23 * tu.folded_abs(pi)).all()
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -281,5 +324,7 @@ def test_ws_and_cluster_paths_agree(w4):
     b32, _, _ = run_gemv(w4, p, packed, path="ws")
     rows = sample_rows(N, np.random.default_rng(15))
     _, refabs = oracle_rows(p, rows)
-    n = (8 + K // 128 + path_splits(w4, "cluster", K, N) + 1) + (8 + K // 128 + K // 128 + 1)
-    assert (np.abs(a32[:, rows].astype(np.float64) - b32[:, rows]) <= n * 2.0 ** -23 * refabs).all()
+    n_cl = 8 + K // 128 + path_splits(w4, "cluster", K, N) + 1 + tu.FOLD_EXTRA_STEPS
+    n_ws = 8 + K // 128 + K // 128 + 1
+    bound = 2.0 ** -23 * (n_cl * tu.folded_abs(p, rows) + n_ws * refabs)
+    assert (np.abs(a32[:, rows].astype(np.float64) - b32[:, rows]) <= bound).all()
