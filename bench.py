@@ -52,17 +52,27 @@ def chain_bytes(layers: int = syn.LAYERS_7B, M: int = 1) -> int:
     return layers * sum(canonical_bytes(M, K, N) for _, K, N in syn.LAYER_7B)
 
 
+KERNEL_SOURCES = ("w4_gemv.cu", "w4_device.cuh", "w4_internal.cuh")
+
+
+def kernel_source_sha() -> str:
+    """sha256 (16 hex digits) of the GEMV kernel's sources, in a fixed order."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "int4_weight_only_w4_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def gemv_traffic():
     """DRAM bytes per gate_up launch from the committed ncu summary, or None
-    when the kernel source has changed since those counters were taken."""
-    import hashlib
+    when the kernel sources have changed since those counters were taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "gemv_traffic.json")) as f:
             rec = json.load(f)
-        with open(os.path.join(ROOT, "int4_weight_only_w4_gb300", "csrc", "w4_gemv.cu"),
-                  "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
-        return rec["traffic_bytes_per_launch"] if sha == rec["w4_gemv_cu_sha256_16"] else None
+        return rec["traffic_bytes_per_launch"] if kernel_source_sha() == rec["kernel_sha256_16"] \
+            else None
     except Exception:
         return None
 
