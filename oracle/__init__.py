@@ -69,6 +69,8 @@ def _load():
     lib.w4o_gemv_f64.argtypes = [P, P, P, P, I, I, I, P, P]
     lib.w4o_gemv_rows_f64.restype = None
     lib.w4o_gemv_rows_f64.argtypes = [P, P, P, P, I, I, P, I, P, P]
+    lib.w4o_quantize.restype = None
+    lib.w4o_quantize.argtypes = [P, I, I, I, P, P, P]
     _lib = lib
     return lib
 
@@ -163,3 +165,20 @@ def gemv_rows_f64(qweight, scales, zeros, x, M: int, K: int, N: int, rows,
     _load().w4o_gemv_rows_f64(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), M, K,
                               _ptr(rows), R, _ptr(y), _ptr(yabs) if with_abs else None)
     return (y, yabs) if with_abs else y
+
+
+QUANT_ASYM = 0      # w4o_quantize mode 0: min/max including 0, zero point per group
+QUANT_SYM = 1       # mode 1: the pages' absmax / 7, zero point fixed at 8
+
+
+def quantize(w, K: int, N: int, mode: int = QUANT_ASYM):
+    """binary16 W[N, K] (bit patterns) -> (qweight [N, K/8] uint32, scales
+    [N, K/128] uint16 (binary16), zeros [N, K/128] uint8), canonical layout."""
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    if w.shape != (N, K) or K % GROUP or mode not in (QUANT_ASYM, QUANT_SYM):
+        raise ValueError("w must be [N, K] with K a multiple of 128, mode 0 or 1")
+    qweight = np.empty((N, K // 8), dtype=np.uint32)
+    scales = np.empty((N, K // GROUP), dtype=np.uint16)
+    zeros = np.empty((N, K // GROUP), dtype=np.uint8)
+    _load().w4o_quantize(_ptr(w), K, N, mode, _ptr(qweight), _ptr(scales), _ptr(zeros))
+    return qweight, scales, zeros

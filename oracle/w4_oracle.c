@@ -197,3 +197,78 @@ void w4o_gemv_rows_f64(const uint32_t *qweight, const uint16_t *scales,
             w4o_dot(qweight, scales, zeros, x, K, (int)rows[i], m,
                     &y[(size_t)m * R + i], yabs ? &yabs[(size_t)m * R + i] : 0);
 }
+
+/* ---- quantisation: binary16 W -> canonical (q, s, z) ------------------------
+ *
+ * Per row n and group g of 128 weights (the grouping of the matrix-vector
+ * product above), in fp32 from the exact binary16 values, every operation
+ * rounded to nearest (ties to even):
+ *
+ *  mode 0, asymmetric (the storage format's zero point, round to nearest):
+ *    lo = min(0, min w), hi = max(0, max w)   -- 0 is always representable
+ *    s  = fp16((hi - lo) / 15)
+ *    z  = clamp(rint(-lo / s), 0, 15)
+ *    q  = clamp(rint(w / s) + z, 0, 15)
+ *  mode 1, symmetric ("Building an LLM Inference Runtime ...", section "The
+ *  Stack Architecture: A One-Page Overview": scale = absmax / 7;
+ *  "CodeAlign-Runtime", section "Level 3 -- Quantization Scheme": values in
+ *  [-8, 7]), stored with the fixed zero point 8:
+ *    s  = fp16(max |w| / 7)
+ *    z  = 8
+ *    q  = clamp(rint(w / s), -8, 7) + 8
+ *
+ * The codes are computed against the stored (fp16) scale, so that (q - z) * s
+ * is the value the product uses.  A group whose scale rounds to 0 (all zeros,
+ * or a range below the smallest fp16 subnormal) stores s = 0 and q = z (0 in
+ * mode 0, 8 in mode 1).  Inputs must be finite.
+ */
+static float w4o_clampf(float v, float a, float b)
+{
+    return v < a ? a : (v > b ? b : v);
+}
+
+void w4o_quantize(const uint16_t *w, int K, int N, int mode, uint32_t *qweight,
+                  uint16_t *scales, uint8_t *zeros)
+{
+    const int G = K / W4O_GROUP;
+    memset(qweight, 0, (size_t)N * (size_t)(K / 8) * sizeof(uint32_t));
+    for (int n = 0; n < N; ++n) {
+        for (int g = 0; g < G; ++g) {
+            const uint16_t *wg = w + (size_t)n * K + (size_t)g * W4O_GROUP;
+            float lo = 0.0f, hi = 0.0f, amax = 0.0f;
+            for (int k = 0; k < W4O_GROUP; ++k) {
+                const float v = (float)w4o_half_to_double(wg[k]);
+                if (v < lo) lo = v;
+                if (v > hi) hi = v;
+                if (fabsf(v) > amax) amax = fabsf(v);
+            }
+            const float s32 = mode == 0 ? (hi - lo) / 15.0f : amax / 7.0f;
+            const uint16_t sh = w4o_double_to_half_rne((double)s32);
+            const float s = (float)w4o_half_to_double(sh);
+            int z;
+            if (s == 0.0f)
+                z = mode == 0 ? 0 : 8;
+            else if (mode == 0)
+                z = (int)w4o_clampf(rintf(-lo / s), 0.0f, 15.0f);
+            else
+                z = 8;
+            for (int k = 0; k < W4O_GROUP; ++k) {
+                int q;
+                if (s == 0.0f) {
+                    q = z;
+                } else {
+                    const float t = rintf((float)w4o_half_to_double(wg[k]) / s);
+                    if (mode == 0)
+                        q = (int)w4o_clampf(w4o_clampf(t, -16.0f, 16.0f) + (float)z, 0.0f,
+                                            15.0f);
+                    else
+                        q = (int)w4o_clampf(t, -8.0f, 7.0f) + 8;
+                }
+                const int kk = g * W4O_GROUP + k;
+                qweight[(size_t)n * (K / 8) + kk / 8] |= (uint32_t)q << (4 * (kk % 8));
+            }
+            scales[(size_t)n * G + g] = sh;
+            zeros[(size_t)n * G + g] = (uint8_t)z;
+        }
+    }
+}

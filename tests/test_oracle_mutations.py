@@ -10,6 +10,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_quantize as qpins
 
 MUTATIONS = {
     "sign of q - z": ("return (float)(q - z) * s;", "return (float)(z - q) * s;"),
@@ -21,6 +22,23 @@ MUTATIONS = {
                                       "(size_t)(k / W4O_GROUP) * (size_t)G + (size_t)n % G"),
 }
 
+QUANT_MUTATIONS = {
+    "asymmetric scale over 16 steps": ("(hi - lo) / 15.0f", "(hi - lo) / 16.0f"),
+    "symmetric scale absmax / 8": ("amax / 7.0f", "amax / 8.0f"),
+    "truncation instead of rounding": ("const float t = rintf(", "const float t = truncf("),
+    "zero point sign flipped": ("rintf(-lo / s)", "rintf(lo / s)"),
+    "zero left out of the range": ("float lo = 0.0f, hi = 0.0f, amax = 0.0f;",
+                                   "float lo = 1e30f, hi = -1e30f, amax = 0.0f;"),
+    "codes against the unrounded scale": ("const float t = rintf((float)w4o_half_to_double(wg[k]) / s);",
+                                          "const float t = rintf((float)w4o_half_to_double(wg[k]) / s32);"),
+}
+
+QUANT_CHECKS = [
+    lambda: [qpins.test_golden_groups(c) for c in qpins._groups()],
+    qpins.test_exactly_representable_groups_round_trip,
+    lambda: qpins.test_modes_agree_on_the_symmetric_special_case(),
+]
+
 PIN_CHECKS = [
     pins.test_golden_nibble_order,
     pins.test_golden_group_index,
@@ -28,6 +46,40 @@ PIN_CHECKS = [
     lambda: pins.test_bruteforce_exact(2, 256, 3, 1),
     pins.test_one_hot_x_exact,
 ]
+
+
+def _caught(old, new, checks, tmp_path):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "w4_oracle.c")).read()
+    assert old in src, "mutation site moved"
+    path = tmp_path / "mut.c"
+    path.write_text(src.replace(old, new, 1))
+    so = tmp_path / "libmut.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-o", str(so), str(path), "-lm"], check=True)
+    saved_lib, saved_path, saved_build = oracle._lib, oracle._LIB_PATH, oracle.build
+    try:
+        oracle._lib = None
+        oracle._LIB_PATH = str(so)
+        oracle.build = lambda force=False, _p=str(so): _p  # noqa: E731 -- load the mutant
+        caught = 0
+        for check in checks:
+            try:
+                check()
+            except AssertionError:
+                caught += 1
+        return caught
+    finally:
+        oracle._lib, oracle._LIB_PATH, oracle.build = saved_lib, saved_path, saved_build
+        import importlib
+        importlib.reload(oracle)
+
+
+@pytest.mark.parametrize("name", sorted(QUANT_MUTATIONS))
+def test_planted_quantiser_mistake_is_caught(name, tmp_path):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    old, new = QUANT_MUTATIONS[name]
+    assert _caught(old, new, QUANT_CHECKS, tmp_path) > 0, f"no pin caught mutation: {name}"
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
