@@ -467,6 +467,71 @@ def per_shape_arm(args):
     return 0
 
 
+QUANT_SHAPES = [("qwen7b.gate_up", 3584, 37888), ("qwen7b.down", 18944, 3584),
+                ("qwen7b.lm_head", 3584, 152064)]
+
+
+def quantize_bytes(K: int, N: int) -> int:
+    """Algorithmic bytes of one w4_quantize call: fp16 W in, canonical
+    nibbles, fp16 scales and uint8 zeros out."""
+    G = K // 128
+    return 2 * N * K + N * K // 2 + 2 * N * G + N * G
+
+
+def quantize_arm(args):
+    """Per-call timing of w4_quantize (both rules) on the weight shapes of the
+    workloads: R calls over rotating input copies (together > 3 x L2) in one
+    CUDA graph, median of 5.  One JSON line per (shape, rule)."""
+    import torch
+
+    from int4_weight_only_w4_gb300 import w4
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    peak, peak_kind = read_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    for name, K, N in QUANT_SHAPES:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(SEED)
+        copies = max(1, -(-3 * l2 // (2 * N * K)))
+        ws = [(torch.randn((N, K), generator=gen, device=dev) * 0.02).half().view(torch.int16)
+              for _ in range(copies)]
+        qw = torch.empty((N, K // 8), dtype=torch.int32, device=dev)
+        sc = torch.empty((N, K // 128), dtype=torch.int16, device=dev)
+        zp = torch.empty((N, K // 128), dtype=torch.uint8, device=dev)
+        for mode, rule in ((w4.QUANT_ASYMMETRIC, "asymmetric"), (w4.QUANT_SYMMETRIC, "symmetric")):
+            reps = max(4, copies)
+            with torch.cuda.stream(stream):
+                w4.quantize(ws[0], K, N, mode, qw, sc, zp, stream=stream)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(reps):
+                    w4.quantize(ws[i % copies], K, N, mode, qw, sc, zp, stream=stream)
+            times = []
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    g.replay()
+                for _ in range(5):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                    e1.synchronize()
+                    times.append(e0.elapsed_time(e1) * 1e3 / reps)
+            us = statistics.median(times)
+            b = quantize_bytes(K, N)
+            print(json.dumps({"op": "w4_quantize", "rule": rule, "shape": name, "K": K, "N": N,
+                              "us_per_call": round(us, 3), "GBps": round(b / us / 1e3, 1),
+                              "frac_of_peak": round(b / us / 1e3 / peak, 4),
+                              "peak_kind": peak_kind, "bytes": b, "copies": copies,
+                              "runs_us": [round(t, 3) for t in times]}), flush=True)
+        del ws, qw, sc, zp
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -475,6 +540,8 @@ def main():
     ap.add_argument("--impl", choices=["w4", "reference"], default="w4")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quantize", action="store_true",
+                    help="per-call timing of w4_quantize on the workloads' weight shapes")
     ap.add_argument("--per-shape", action="store_true",
                     help="per-call timing of every workload shape instead of the chain")
     ap.add_argument("--kernel-case", default=None,
@@ -484,6 +551,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return reference_arm(args)
+    if args.quantize:
+        return quantize_arm(args)
     if args.per_shape or args.kernel_case:
         return per_shape_arm(args)
     return gpu_arm(args)

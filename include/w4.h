@@ -230,6 +230,39 @@ w4_status w4_gemv_ws_static(const void *qweight, const void *scales, const void 
                             const uint16_t *x, uint16_t *y, int M, int K, int N,
                             w4_stream_t stream);
 
+/* Quantisation rules for w4_quantize. */
+#define W4_QUANT_ASYMMETRIC 0
+#define W4_QUANT_SYMMETRIC 1
+
+/*
+ * Quantise binary16 weights to the canonical layout, per row and group of
+ * 128 consecutive weights along K, computing in fp32 from the exact binary16
+ * values with every operation rounded to nearest (ties to even); the codes
+ * are taken against the stored fp16 scale, so (q - z) * s is the value the
+ * product uses:
+ *   W4_QUANT_ASYMMETRIC: lo = min(0, min w), hi = max(0, max w),
+ *     s = fp16((hi - lo) / 15), z = clamp(rint(-lo / s), 0, 15),
+ *     q = clamp(rint(w / s) + z, 0, 15)  (round to nearest with a zero point
+ *     per group: the storage format of this library);
+ *   W4_QUANT_SYMMETRIC: s = fp16(max |w| / 7), z = 8,
+ *     q = clamp(rint(w / s), -8, 7) + 8  (the pages' scheme: scale = absmax
+ *     / 7, "Building an LLM Inference Runtime ...", section "The Stack
+ *     Architecture: A One-Page Overview"; values in [-8, 7],
+ *     "CodeAlign-Runtime", section "Level 3 -- INT4 Quantization + Fused
+ *     Kernel"; stored with the fixed zero point 8).
+ * A group whose scale rounds to 0 stores s = 0 and q = z.
+ *
+ *   w       : device, binary16 bit patterns [N][K], 16-byte aligned; finite
+ *   mode    : W4_QUANT_ASYMMETRIC or W4_QUANT_SYMMETRIC
+ *   qweight : device, uint32 [N][K/8] (canonical nibble order), 4-byte aligned
+ *   scales  : device, binary16 [N][K/128], 2-byte aligned
+ *   zeros   : device, uint8 [N][K/128]
+ * Outputs are written completely; w4_repack then gives the kernel layout.
+ * Errors: W4_ERR_INVALID_ARG (bad pointers, sizes or mode), W4_ERR_CUDA.
+ */
+w4_status w4_quantize(const uint16_t *w, int K, int N, int mode, uint32_t *qweight,
+                      uint16_t *scales, uint8_t *zeros, w4_stream_t stream);
+
 /*
  * The launch shape w4_gemv uses for an N x K weight on the current device:
  * 16-row tiles per thread block, the number of K splits (thread blocks of

@@ -162,6 +162,19 @@ w4_status w4_gemv_ws_f32(const void *qweight, const void *scales, const void *ze
                           workspace_bytes, stream);
 }
 
+w4_status w4_quantize(const uint16_t *w, int K, int N, int mode, uint32_t *qweight,
+                      uint16_t *scales, uint8_t *zeros, w4_stream_t stream) {
+    if (!w || !qweight || !scales || !zeros) return W4_ERR_INVALID_ARG;
+    if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
+    if (mode != W4_QUANT_ASYMMETRIC && mode != W4_QUANT_SYMMETRIC) return W4_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(qweight, 4) || !aligned(scales, 2))
+        return W4_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return W4_ERR_CUDA;
+    return cuda_status(w4::launch_quantize(w, K, N, mode == W4_QUANT_SYMMETRIC, qweight, scales,
+                                           zeros, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 w4_status w4_gemv_config(int K, int N, int *tiles_per_block, int *k_splits,
                          int *zero_point_folded) {
     if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;

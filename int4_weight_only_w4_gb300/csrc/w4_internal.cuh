@@ -73,6 +73,8 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
 // Workspace path (w4_gemv_sk.cu): grid size, workspace bytes, launch.
 int gemv_ws_blocks(int K, int N, int num_sms);
 size_t gemv_ws_bytes(int K, int N, int num_sms);
+cudaError_t launch_quantize(const uint16_t *w, int K, int N, bool symmetric, uint32_t *qweight,
+                            uint16_t *scales, uint8_t *zeros, int num_sms, cudaStream_t stream);
 cudaError_t launch_gemv_ws(const void *qweight, const void *scales, const void *zeros,
                            const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
                            void *workspace, int num_sms, cudaStream_t stream);

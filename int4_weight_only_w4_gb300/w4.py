@@ -49,6 +49,7 @@ _check_header = _decl("w4_check_header", _ST, _P, _I, _I)
 _dequant = _decl("w4_dequant", _ST, _P, _P, _P, _I, _I, _P, _P)
 _gemv = _decl("w4_gemv", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_f32 = _decl("w4_gemv_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
+_quantize = _decl("w4_quantize", _ST, _P, _I, _I, _I, _P, _P, _P, _P)
 _gemv_ws_static = _decl("w4_gemv_ws_static", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_config = _decl("w4_gemv_config", _ST, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
                      ctypes.POINTER(_I))
@@ -191,6 +192,16 @@ def gemv_ws_static(qweight, scales, zeros, x, y, M: int, K: int, N: int, stream=
     the first call on a device should come before any stream capture."""
     _ok(_gemv_ws_static(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, N,
                         _stream(stream, x)), "w4_gemv_ws_static")
+
+
+QUANT_ASYMMETRIC = 0      # W4_QUANT_ASYMMETRIC
+QUANT_SYMMETRIC = 1       # W4_QUANT_SYMMETRIC
+
+
+def quantize(w, K: int, N: int, mode: int, qweight, scales, zeros, stream=None) -> None:
+    """w4_quantize: binary16 W [N, K] -> canonical qweight, scales, zeros."""
+    _ok(_quantize(_ptr(w), K, N, int(mode), _ptr(qweight), _ptr(scales), _ptr(zeros),
+                  _stream(stream, w)), "w4_quantize")
 
 
 def gemv_config(K: int, N: int):
