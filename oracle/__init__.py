@@ -69,6 +69,8 @@ def _load():
     lib.w4o_gemv_f64.argtypes = [P, P, P, P, I, I, I, P, P]
     lib.w4o_gemv_rows_f64.restype = None
     lib.w4o_gemv_rows_f64.argtypes = [P, P, P, P, I, I, P, I, P, P]
+    lib.w4o_gemv_swiglu_f64.restype = None
+    lib.w4o_gemv_swiglu_f64.argtypes = [P, P, P, P, I, I, I, P]
     lib.w4o_quantize.restype = None
     lib.w4o_quantize.argtypes = [P, I, I, I, P, P, P]
     _lib = lib
@@ -182,3 +184,16 @@ def quantize(w, K: int, N: int, mode: int = QUANT_ASYM):
     zeros = np.empty((N, K // GROUP), dtype=np.uint8)
     _load().w4o_quantize(_ptr(w), K, N, mode, _ptr(qweight), _ptr(scales), _ptr(zeros))
     return qweight, scales, zeros
+
+
+def gemv_swiglu_f64(qweight, scales, zeros, x, M: int, K: int, I: int):
+    """y[M, I] = silu(gate . x) * (up . x) in fp64 for the fused [2I, K] weight
+    (gate rows 0..I-1, up rows I..2I-1)."""
+    qweight, scales, zeros = _check(qweight, scales, zeros, K, 2 * I)
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    if x.shape != (M, K):
+        raise ValueError("x must be [M, K]")
+    y = np.empty((M, I), dtype=np.float64)
+    _load().w4o_gemv_swiglu_f64(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), M, K, I,
+                                _ptr(y))
+    return y

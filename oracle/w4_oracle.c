@@ -272,3 +272,26 @@ void w4o_quantize(const uint16_t *w, int K, int N, int mode, uint32_t *qweight,
         }
     }
 }
+
+/* ---- gate/up product with the SwiGLU activation -----------------------------
+ *
+ * W is the fused [2I][K] matrix of a gated MLP: rows 0..I-1 are the gate
+ * projection, rows I..2I-1 the up projection.  For token m and output j:
+ *   g = sum_k w32(j, k) x[m][k],  u = sum_k w32(I + j, k) x[m][k]  (fp64, as above)
+ *   y[m][j] = silu(g) * u,  silu(g) = g / (1 + exp(-g))
+ * ("qengine", section "How it works": gate and up projections interleaved so
+ * that SwiGLU runs in registers -- the activation applied to the pair of
+ * products of the same output).  fp64 throughout; exp from the C library.
+ */
+void w4o_gemv_swiglu_f64(const uint32_t *qweight, const uint16_t *scales,
+                         const uint8_t *zeros, const uint16_t *x, int M, int K, int I,
+                         double *y)
+{
+    for (int m = 0; m < M; ++m)
+        for (int j = 0; j < I; ++j) {
+            double g, u;
+            w4o_dot(qweight, scales, zeros, x, K, j, m, &g, 0);
+            w4o_dot(qweight, scales, zeros, x, K, I + j, m, &u, 0);
+            y[(size_t)m * I + j] = g / (1.0 + exp(-g)) * u;
+        }
+}

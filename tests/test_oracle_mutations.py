@@ -11,6 +11,7 @@ import pytest
 import oracle
 from tests import test_oracle_pins as pins
 from tests import test_oracle_quantize as qpins
+from tests import test_oracle_swiglu as spins
 
 MUTATIONS = {
     "sign of q - z": ("return (float)(q - z) * s;", "return (float)(z - q) * s;"),
@@ -38,6 +39,15 @@ QUANT_CHECKS = [
     qpins.test_exactly_representable_groups_round_trip,
     lambda: qpins.test_modes_agree_on_the_symmetric_special_case(),
 ]
+
+SWIGLU_MUTATIONS = {
+    "exp of +g": ("g / (1.0 + exp(-g)) * u", "g / (1.0 + exp(g)) * u"),
+    "up row off by one": ("K, I + j, m, &u, 0)", "K, I + j - (j > 0), m, &u, 0)"),
+    "activation on the up product": ("g / (1.0 + exp(-g)) * u", "u / (1.0 + exp(-u)) * g"),
+}
+
+SWIGLU_CHECKS = [spins.test_golden_points, spins.test_odd_part_identity_and_zero_up,
+                 spins.test_gate_row_j_pairs_with_up_row_I_plus_j]
 
 PIN_CHECKS = [
     pins.test_golden_nibble_order,
@@ -72,6 +82,14 @@ def _caught(old, new, checks, tmp_path):
         oracle._lib, oracle._LIB_PATH, oracle.build = saved_lib, saved_path, saved_build
         import importlib
         importlib.reload(oracle)
+
+
+@pytest.mark.parametrize("name", sorted(SWIGLU_MUTATIONS))
+def test_planted_swiglu_mistake_is_caught(name, tmp_path):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    old, new = SWIGLU_MUTATIONS[name]
+    assert _caught(old, new, SWIGLU_CHECKS, tmp_path) > 0, f"no pin caught mutation: {name}"
 
 
 @pytest.mark.parametrize("name", sorted(QUANT_MUTATIONS))
