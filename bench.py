@@ -467,6 +467,86 @@ def per_shape_arm(args):
     return 0
 
 
+SWIGLU_SHAPES = [("qwen7b.gate_up", 3584, 18944, (1, 8), (0.001, 0.02)),
+                 ("27b.gate_up", 5120, 8704, (1, 8), (0.0005, 0.01)),
+                 ("qwen0.5b.gate_up", 896, 4864, (1,), (0.001, 0.02))]
+
+
+def swiglu_bytes(M: int, K: int, I: int) -> int:
+    """Algorithmic bytes of one fused gate/up + SwiGLU call: the [2I, K]
+    weight, x and the I-wide output."""
+    return canonical_bytes(M, K, 2 * I) - 2 * M * I
+
+
+def swiglu_arm(args):
+    """Per-call timing of w4_gemv_swiglu against the plain w4_gemv of the same
+    fused [2I, K] weight: R calls over rotating weight copies (together
+    > 3 x L2) in one CUDA graph, median of 5.  One JSON line per (shape, M)."""
+    import torch
+
+    from int4_weight_only_w4_gb300 import w4
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    peak, peak_kind = read_peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    def timed(fn, reps):
+        with torch.cuda.stream(stream):
+            fn(0)
+            fn(1)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(reps):
+                fn(i)
+        times = []
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                g.replay()
+            for _ in range(5):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1) * 1e3 / reps)
+        return statistics.median(times), times
+
+    for name, K, I, Ms, srange in SWIGLU_SHAPES:
+        qw, sc, zp = syn.make_weights(f"{name}.swiglu", K, 2 * I, SEED, srange)
+        tq = torch.from_numpy(qw.view(np.int32)).to(dev)
+        ts = torch.from_numpy(sc.view(np.int16)).to(dev)
+        tz = torch.from_numpy(zp).to(dev)
+        fused = w4.pack_swiglu(tq, ts, tz, K, I)
+        plain = w4.pack(tq, ts, tz, K, 2 * I)
+        footprint = sum(t.numel() for t in (fused.qweight, fused.scales, fused.zeros))
+        copies = min(4096, max(2, -(-3 * l2 // footprint) + 1))
+        fcopies = [fused] + [w4.PackedSwiGLU(K, I, fused.qweight.clone(), fused.scales.clone(),
+                                             fused.zeros.clone()) for _ in range(copies - 1)]
+        pcopies = [plain] + [w4.PackedWeight(K, 2 * I, plain.qweight.clone(), plain.scales.clone(),
+                                             plain.zeros.clone()) for _ in range(copies - 1)]
+        for M in Ms:
+            x = torch.from_numpy(syn.make_x(f"{name}.swiglu.M{M}", M, K, SEED).view(np.int16)) \
+                .to(dev).view(torch.bfloat16)
+            yf = torch.empty((M, I), dtype=torch.bfloat16, device=dev)
+            yp = torch.empty((M, 2 * I), dtype=torch.bfloat16, device=dev)
+            reps = max(1, -(-64 // copies)) * copies
+            us_f, runs_f = timed(lambda i: fcopies[i % copies].gemv(x, yf, stream=stream), reps)
+            us_p, _ = timed(lambda i: pcopies[i % copies].gemv(x, yp, stream=stream), reps)
+            b = swiglu_bytes(M, K, I)
+            print(json.dumps({"op": "w4_gemv_swiglu", "shape": name, "M": M, "K": K, "I": I,
+                              "us_per_call": round(us_f, 3), "GBps": round(b / us_f / 1e3, 1),
+                              "frac_of_peak": round(b / us_f / 1e3 / peak, 4),
+                              "peak_kind": peak_kind, "bytes": b,
+                              "plain_gemv_us": round(us_p, 3), "copies": copies,
+                              "runs_us": [round(t, 3) for t in runs_f]}), flush=True)
+        del fcopies, pcopies, fused, plain, tq, ts, tz
+        torch.cuda.empty_cache()
+    return 0
+
+
 QUANT_SHAPES = [("qwen7b.gate_up", 3584, 37888), ("qwen7b.down", 18944, 3584),
                 ("qwen7b.lm_head", 3584, 152064)]
 
@@ -540,6 +620,8 @@ def main():
     ap.add_argument("--impl", choices=["w4", "reference"], default="w4")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--swiglu", action="store_true",
+                    help="per-call timing of the fused gate/up + SwiGLU product")
     ap.add_argument("--quantize", action="store_true",
                     help="per-call timing of w4_quantize on the workloads' weight shapes")
     ap.add_argument("--per-shape", action="store_true",
@@ -553,6 +635,8 @@ def main():
         return reference_arm(args)
     if args.quantize:
         return quantize_arm(args)
+    if args.swiglu:
+        return swiglu_arm(args)
     if args.per_shape or args.kernel_case:
         return per_shape_arm(args)
     return gpu_arm(args)

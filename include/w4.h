@@ -59,6 +59,7 @@ typedef enum w4_status {
 #define W4_GROUP_SIZE 128
 #define W4_MAX_TOKENS 8
 #define W4_LAYOUT_ID 1
+#define W4_LAYOUT_ID_SWIGLU 2      /* gate/up-interleaved layout (w4_repack_swiglu) */
 #define W4_LAYOUT_VERSION 3
 #define W4_HEADER_BYTES 128
 /* Size of the static device array behind w4_gemv_ws_static (4 MiB). */
@@ -229,6 +230,43 @@ w4_status w4_gemv_ws_f32(const void *qweight, const void *scales, const void *ze
 w4_status w4_gemv_ws_static(const void *qweight, const void *scales, const void *zeros,
                             const uint16_t *x, uint16_t *y, int M, int K, int N,
                             w4_stream_t stream);
+
+/*
+ * Gated MLP input projection with the SwiGLU activation fused into the
+ * product ("qengine", section "How it works": gate and up projections
+ * interleaved so that SwiGLU runs in registers).  The weight is the fused
+ * [2I][K] matrix of the gate projection (rows 0..I-1) and the up projection
+ * (rows I..2I-1), canonical layout as above; the result is
+ *   y[m][j] = silu(g) * u,  g = sum_k Wgate[j][k] x[m][k],
+ *   u = sum_k Wup[j][k] x[m][k],  silu(g) = g / (1 + exp(-g)),
+ * with g and u accumulated exactly as by w4_gemv_f32 and the activation and
+ * product in fp32.
+ *
+ * w4_repacked_sizes_swiglu: byte sizes of the three buffers of the
+ *   interleaved layout for I outputs (16 * ceil(I / 8) kernel rows).
+ * w4_repack_swiglu: as w4_repack, for the fused [2I][K] weight (qweight
+ *   uint32 [2I][K/8], scales [2I][K/128], zeros [2I][K/128]); the header
+ *   records layout W4_LAYOUT_ID_SWIGLU and N = I.  Synchronises; refuses
+ *   stream capture (W4_ERR_UNSUPPORTED); zero points > 15 -> W4_ERR_INVALID_ARG.
+ * w4_check_header_swiglu: as w4_check_header for that layout and I.
+ * w4_gemv_swiglu: y bfloat16 [M][I] (round to nearest even); arguments as
+ *   for w4_gemv with N replaced by I; the weight buffers must come from
+ *   w4_repack_swiglu.  w4_gemv_swiglu_f32: the fp32 result.
+ * Errors: W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED (M outside 1..8),
+ * W4_ERR_CUDA.
+ */
+w4_status w4_repacked_sizes_swiglu(int K, int I, size_t *qweight_bytes, size_t *scales_bytes,
+                                   size_t *zeros_bytes);
+w4_status w4_repack_swiglu(const uint32_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                           int K, int I, void *qweight_out, void *scales_out, void *zeros_out,
+                           w4_stream_t stream);
+w4_status w4_check_header_swiglu(const void *header, int K, int I);
+w4_status w4_gemv_swiglu(const void *qweight, const void *scales, const void *zeros,
+                         const uint16_t *x, uint16_t *y, int M, int K, int I,
+                         w4_stream_t stream);
+w4_status w4_gemv_swiglu_f32(const void *qweight, const void *scales, const void *zeros,
+                             const uint16_t *x, float *y, int M, int K, int I,
+                             w4_stream_t stream);
 
 /* Quantisation rules for w4_quantize. */
 #define W4_QUANT_ASYMMETRIC 0

@@ -37,8 +37,61 @@ w4_status gemv_common(const void *qweight, const void *scales, const void *zeros
     if (sms <= 0) return W4_ERR_CUDA;
     w4::GemvShape shape;
     if (!w4::gemv_shape(K, N, sms, &shape)) return W4_ERR_UNSUPPORTED;
-    return cuda_status(w4::launch_gemv(qweight, scales, zeros, x, y, f32_out, M, K, N, shape,
+    return cuda_status(w4::launch_gemv(qweight, scales, zeros, x, y, f32_out, M, K, N, shape, 0,
                                        sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+w4_status repack_common(const uint32_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                        int K, int N, int swiglu_I, void *qweight_out, void *scales_out,
+                        void *zeros_out, w4_stream_t stream) {
+    if (!qweight || !scales || !zeros || !qweight_out || !scales_out || !zeros_out)
+        return W4_ERR_INVALID_ARG;
+    if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
+    if (!aligned(qweight, 4) || !aligned(scales, 2) || !aligned(qweight_out, 16) ||
+        !aligned(scales_out, 16) || !aligned(zeros_out, 16))
+        return W4_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return W4_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return W4_ERR_UNSUPPORTED;
+    cudaError_t e = w4::launch_repack(qweight, scales, zeros, K, N, swiglu_I, qweight_out,
+                                      scales_out, zeros_out, s);
+    if (e != cudaSuccess) return W4_ERR_CUDA;
+    w4::Header h;
+    e = cudaMemcpyAsync(&h, qweight_out, sizeof h, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return W4_ERR_CUDA;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return W4_ERR_CUDA;
+    return h.bad_zeros ? W4_ERR_INVALID_ARG : W4_OK;
+}
+
+w4_status check_header_common(const void *header, int K, int N, uint32_t layout_id) {
+    if (!header) return W4_ERR_INVALID_ARG;
+    w4::Header h;
+    memcpy(&h, header, sizeof h);
+    if (memcmp(h.magic, "W4G128KL", 8) != 0 || h.layout_id != layout_id ||
+        h.version != W4_LAYOUT_VERSION || h.K != K || h.N != N || h.bad_zeros != 0)
+        return W4_ERR_LAYOUT;
+    if (h.kernel_error != 0) return W4_ERR_CUDA;
+    return W4_OK;
+}
+
+w4_status gemv_swiglu_common(const void *qweight, const void *scales, const void *zeros,
+                             const uint16_t *x, void *y, bool f32_out, int M, int K, int I,
+                             w4_stream_t stream) {
+    if (!qweight || !scales || !zeros || !x || !y) return W4_ERR_INVALID_ARG;
+    if (!valid_kn(K, I)) return W4_ERR_INVALID_ARG;
+    if (M < 1 || M > W4_MAX_TOKENS) return W4_ERR_UNSUPPORTED;
+    if (!aligned(qweight, 16) || !aligned(scales, 16) || !aligned(zeros, 16) ||
+        !aligned(x, 16) || !aligned(y, f32_out ? 4 : 2))
+        return W4_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return W4_ERR_CUDA;
+    const int rows = w4::swiglu_rows(I);
+    w4::GemvShape shape;
+    if (!w4::gemv_shape(K, rows, sms, &shape)) return W4_ERR_UNSUPPORTED;
+    return cuda_status(w4::launch_gemv(qweight, scales, zeros, x, y, f32_out, M, K, rows, shape,
+                                       I, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 w4_status gemv_ws_common(const void *qweight, const void *scales, const void *zeros,
@@ -88,36 +141,42 @@ w4_status w4_repacked_sizes(int K, int N, size_t *qweight_bytes, size_t *scales_
 w4_status w4_repack(const uint32_t *qweight, const uint16_t *scales, const uint8_t *zeros, int K,
                     int N, void *qweight_out, void *scales_out, void *zeros_out,
                     w4_stream_t stream) {
-    if (!qweight || !scales || !zeros || !qweight_out || !scales_out || !zeros_out)
-        return W4_ERR_INVALID_ARG;
-    if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
-    if (!aligned(qweight, 4) || !aligned(scales, 2) || !aligned(qweight_out, 16) ||
-        !aligned(scales_out, 16) || !aligned(zeros_out, 16))
-        return W4_ERR_INVALID_ARG;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return W4_ERR_CUDA;
-    if (cap != cudaStreamCaptureStatusNone) return W4_ERR_UNSUPPORTED;
-    cudaError_t e = w4::launch_repack(qweight, scales, zeros, K, N, qweight_out, scales_out,
-                                      zeros_out, s);
-    if (e != cudaSuccess) return W4_ERR_CUDA;
-    w4::Header h;
-    e = cudaMemcpyAsync(&h, qweight_out, sizeof h, cudaMemcpyDeviceToHost, s);
-    if (e != cudaSuccess) return W4_ERR_CUDA;
-    e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return W4_ERR_CUDA;
-    return h.bad_zeros ? W4_ERR_INVALID_ARG : W4_OK;
+    return repack_common(qweight, scales, zeros, K, N, 0, qweight_out, scales_out, zeros_out,
+                         stream);
 }
 
 w4_status w4_check_header(const void *header, int K, int N) {
-    if (!header) return W4_ERR_INVALID_ARG;
-    w4::Header h;
-    memcpy(&h, header, sizeof h);
-    if (memcmp(h.magic, "W4G128KL", 8) != 0 || h.layout_id != W4_LAYOUT_ID ||
-        h.version != W4_LAYOUT_VERSION || h.K != K || h.N != N || h.bad_zeros != 0)
-        return W4_ERR_LAYOUT;
-    if (h.kernel_error != 0) return W4_ERR_CUDA;
-    return W4_OK;
+    return check_header_common(header, K, N, W4_LAYOUT_ID);
+}
+
+w4_status w4_repacked_sizes_swiglu(int K, int I, size_t *qweight_bytes, size_t *scales_bytes,
+                                   size_t *zeros_bytes) {
+    if (!valid_kn(K, I) || I > (1 << 29)) return W4_ERR_INVALID_ARG;
+    return w4_repacked_sizes(K, w4::swiglu_rows(I), qweight_bytes, scales_bytes, zeros_bytes);
+}
+
+w4_status w4_repack_swiglu(const uint32_t *qweight, const uint16_t *scales, const uint8_t *zeros,
+                           int K, int I, void *qweight_out, void *scales_out, void *zeros_out,
+                           w4_stream_t stream) {
+    if (!valid_kn(K, I) || I > (1 << 29)) return W4_ERR_INVALID_ARG;
+    return repack_common(qweight, scales, zeros, K, w4::swiglu_rows(I), I, qweight_out,
+                         scales_out, zeros_out, stream);
+}
+
+w4_status w4_check_header_swiglu(const void *header, int K, int I) {
+    return check_header_common(header, K, I, W4_LAYOUT_ID_SWIGLU);
+}
+
+w4_status w4_gemv_swiglu(const void *qweight, const void *scales, const void *zeros,
+                         const uint16_t *x, uint16_t *y, int M, int K, int I,
+                         w4_stream_t stream) {
+    return gemv_swiglu_common(qweight, scales, zeros, x, y, false, M, K, I, stream);
+}
+
+w4_status w4_gemv_swiglu_f32(const void *qweight, const void *scales, const void *zeros,
+                             const uint16_t *x, float *y, int M, int K, int I,
+                             w4_stream_t stream) {
+    return gemv_swiglu_common(qweight, scales, zeros, x, y, true, M, K, I, stream);
 }
 
 w4_status w4_dequant(const uint32_t *qweight, const uint16_t *scales, const uint8_t *zeros, int K,

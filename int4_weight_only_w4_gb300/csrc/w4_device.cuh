@@ -229,6 +229,31 @@ __device__ __forceinline__ void group_mma_folded(float (&acc)[4], const GroupDat
     acc[3] = fmaf(fmaf(nzh, xs.y, d[0][3] + d[1][3]), sh, acc[3]);
 }
 
+// The SwiGLU epilogue of the gate/up-interleaved layout: tile t holds gate
+// rows 8t..8t+7 in its rows gq and the matching up rows in gq + 8, so the
+// lane's acc[0], acc[2] (token 2tq) and acc[1], acc[3] (token 2tq + 1) are
+// (gate, up) pairs of output j = 8t + gq: y[m][j] = silu(gate) * up in fp32.
+template <bool F32OUT>
+__device__ __forceinline__ void store_swiglu(void *yv, const float (&acc)[4], int t, int lane,
+                                             int M, int I) {
+    const int gq = lane >> 2, tq = lane & 3;
+    const int j = 8 * t + gq;
+    if (j >= I) return;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int m = 2 * tq + h;
+        if (m < M) {
+            const float g = acc[h], u = acc[2 + h];
+            const float v = g / (1.f + expf(-g)) * u;
+            const size_t o = (size_t)m * I + j;
+            if (F32OUT)
+                static_cast<float *>(yv)[o] = v;
+            else
+                static_cast<__nv_bfloat16 *>(yv)[o] = __float2bfloat16_rn(v);
+        }
+    }
+}
+
 template <bool F32OUT>
 __device__ __forceinline__ void store_tile(void *yv, const float (&acc)[4], int t, int lane,
                                            int M, int N) {

@@ -89,10 +89,20 @@ __host__ __device__ inline SmemPlan smem_plan(int K, int S, int M) {
 // partials visible, and each reducing warp adds its S slots from its own
 // shared memory.  No block reads another block's memory after the barrier,
 // so none has to wait for the others before exiting.
+// Final store of a tile: y = W x, or the SwiGLU of the interleaved pairs.
+template <bool F32OUT>
+__device__ __forceinline__ void store_out(void *yv, const float (&acc)[4], int t, int lane, int M,
+                                          int N, int swiglu_I) {
+    if (swiglu_I)
+        store_swiglu<F32OUT>(yv, acc, t, lane, M, swiglu_I);
+    else
+        store_tile<F32OUT>(yv, acc, t, lane, M, N);
+}
+
 template <bool F32OUT>
 __device__ __forceinline__ void cluster_combine(float a0, float a1, float a2, float a3, void *yv,
                                              unsigned char *red_bytes, int t, int S, int split,
-                                             int M, int N) {
+                                             int M, int N, int swiglu_I) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int J = (kWarps + S - 1) / S;                 // tiles reduced per block
     float4 *red = reinterpret_cast<float4 *>(red_bytes);
@@ -112,7 +122,7 @@ __device__ __forceinline__ void cluster_combine(float a0, float a1, float a2, fl
             s3 += v.w;
         }
         const float tot[4] = {s0, s1, s2, s3};
-        store_tile<F32OUT>(yv, tot, t, lane, M, N);
+        store_out<F32OUT>(yv, tot, t, lane, M, N, swiglu_I);
     }
 }
 
@@ -121,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
 gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             const char *__restrict__ zp, const __nv_bfloat16 *__restrict__ x,
             void *__restrict__ yv, uint32_t *err, int M, int K, int N, int S, int pre,
+            int swiglu_I,
             uint32_t nib_mask, uint32_t bf16_magic) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int G = K / kGroup;
@@ -348,11 +359,11 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
     wait_prerequisites();       // y may be read by the previous kernel in the stream
     const int t = b * kWarps + warp;
     if (S == 1) {
-        if (warp < kWarps && ok) store_tile<F32OUT>(yv, acc, t, lane, M, N);
+        if (warp < kWarps && ok) store_out<F32OUT>(yv, acc, t, lane, M, N, swiglu_I);
         return;
     }
     cluster_combine<F32OUT>(acc[0], acc[1], acc[2], acc[3], yv, smem + plan.red_off, t, S, split,
-                            M, N);
+                            M, N, swiglu_I);
 }
 
 }  // namespace
@@ -437,7 +448,8 @@ int active_clusters(const void *kern, cudaLaunchConfig_t cfg, int dev) {
 
 cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zeros,
                         const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
-                        const GemvShape &shape, int num_sms, cudaStream_t stream) {
+                        const GemvShape &shape, int swiglu_I, int num_sms,
+                        cudaStream_t stream) {
     const int S = shape.splits;
     // Small M: x is small, so three blocks fit per SM (more warps to hide
     // latency).  The split S, and so the arithmetic, is the same either way.
@@ -450,7 +462,8 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const DeviceSmem &ds = device_smem(dev);
     using Kern = void (*)(const char *, const char *, const char *, const __nv_bfloat16 *,
-                          void *, uint32_t *, int, int, int, int, int, uint32_t, uint32_t);
+                          void *, uint32_t *, int, int, int, int, int, int, uint32_t,
+                          uint32_t);
     static const Kern kKernels[2][2][2] = {
         {{gemv_kernel<false, 2, false>, gemv_kernel<false, 2, true>},
          {gemv_kernel<false, 3, false>, gemv_kernel<false, 3, true>}},
@@ -520,7 +533,7 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     return cudaLaunchKernelEx(&cfg, kern, q, static_cast<const char *>(scales),
                               static_cast<const char *>(zeros),
                               reinterpret_cast<const __nv_bfloat16 *>(x), y, err, M, K, N, S,
-                              overlap ? 2 : 0, 0x000F000Fu, 0x43004300u);
+                              overlap ? 2 : 0, swiglu_I, 0x000F000Fu, 0x43004300u);
 }
 
 }  // namespace w4

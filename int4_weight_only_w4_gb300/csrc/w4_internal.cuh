@@ -34,6 +34,10 @@ struct Header {
 static_assert(sizeof(Header) == W4_HEADER_BYTES, "header size");
 
 __host__ __device__ inline int row_blocks(int N) { return (N + kBlockRows - 1) / kBlockRows; }
+
+// Rows of the gate/up-interleaved layout for I outputs: every 16-row tile
+// holds 8 gate rows and the 8 matching up rows (see w4_repack.cu).
+__host__ __device__ inline int swiglu_rows(int I) { return 16 * ((I + 7) / 8); }
 constexpr size_t kErrorOffset = 28;   // byte offset of Header::kernel_error
 
 // Kernel-layout byte sizes (see w4_repack.cu for the layout itself).
@@ -47,8 +51,10 @@ inline size_t packed_zeros_bytes(int K, int N) {
     return (size_t)row_blocks(N) * (K / kGroup) * kRecZeros;
 }
 
+// swiglu_I = 0: plain layout of an N x K weight.  swiglu_I = I > 0: the
+// input is a fused [2I][K] gate/up weight and N must be swiglu_rows(I).
 cudaError_t launch_repack(const uint32_t *qweight, const uint16_t *scales,
-                          const uint8_t *zeros, int K, int N, void *qweight_out,
+                          const uint8_t *zeros, int K, int N, int swiglu_I, void *qweight_out,
                           void *scales_out, void *zeros_out, cudaStream_t stream);
 
 cudaError_t launch_dequant(const uint32_t *qweight, const uint16_t *scales,
@@ -66,9 +72,12 @@ struct GemvShape {
 // shape fits the shared-memory budget.
 bool gemv_shape(int K, int N, int num_sms, GemvShape *out);
 
+// swiglu_I = 0: y[M][N] = W x.  swiglu_I = I > 0: W is a gate/up-interleaved
+// weight of N = swiglu_rows(I) rows and y[M][I] = silu(gate x) * (up x).
 cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zeros,
                         const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
-                        const GemvShape &shape, int num_sms, cudaStream_t stream);
+                        const GemvShape &shape, int swiglu_I, int num_sms,
+                        cudaStream_t stream);
 
 // Workspace path (w4_gemv_sk.cu): grid size, workspace bytes, launch.
 int gemv_ws_blocks(int K, int N, int num_sms);

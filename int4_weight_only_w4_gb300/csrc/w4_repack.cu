@@ -33,6 +33,14 @@
 //   zeros:   64 B at (b*G + g) * 64: byte [w][gq] = z of row 16t+gq (low
 //            nibble) | z of row 16t+gq+8 (high nibble).
 // Padded rows have q = z = 0 and s = 0, so they contribute exact zeros.
+//
+// Gate/up-interleaved layout (layout id W4_LAYOUT_ID_SWIGLU): the input is a
+// fused [2I][K] weight (gate rows 0..I-1, up rows I..2I-1) and kernel row
+// r = 16 t + i holds gate row 8t + i for i < 8 and up row 8t + i - 8 for
+// i >= 8 (zero past I).  Each lane of the tensor-core operation then holds,
+// for rows gq and gq + 8 of a tile, the gate and the up product of the same
+// output, so the activation runs in registers ("qengine", section "How it
+// works": gate and up projections interleaved so SwiGLU runs in registers).
 #include <string.h>
 
 #include "w4_internal.cuh"
@@ -40,10 +48,10 @@
 namespace w4 {
 namespace {
 
-__global__ void write_header_kernel(Header *h, int K, int N) {
+__global__ void write_header_kernel(Header *h, int K, int N, uint32_t layout_id) {
     const char magic[8] = {'W', '4', 'G', '1', '2', '8', 'K', 'L'};
     for (int i = 0; i < 8; ++i) h->magic[i] = magic[i];
-    h->layout_id = W4_LAYOUT_ID;
+    h->layout_id = layout_id;
     h->version = W4_LAYOUT_VERSION;
     h->K = K;
     h->N = N;
@@ -54,8 +62,16 @@ __global__ void write_header_kernel(Header *h, int K, int N) {
 
 __device__ __forceinline__ uint32_t nib(uint32_t w, int i) { return (w >> (4 * i)) & 0xFu; }
 
+// Canonical row of kernel row r, or -1 for a zero row.
+__device__ __forceinline__ int src_row(int r, int N, int swiglu_I) {
+    if (swiglu_I == 0) return r < N ? r : -1;
+    const int j = 8 * (r >> 4) + (r & 7);
+    if (j >= swiglu_I) return -1;
+    return (r & 8) ? swiglu_I + j : j;
+}
+
 __global__ void repack_weights_kernel(const uint32_t *__restrict__ qw, int K, int N, int NB,
-                                      uint4 *__restrict__ out) {
+                                      int swiglu_I, uint4 *__restrict__ out) {
     const int G = K / kGroup;
     const size_t words_per_row = (size_t)K / 8;
     const size_t total = (size_t)NB * G * (kRecWeights / 16);
@@ -68,15 +84,16 @@ __global__ void repack_weights_kernel(const uint32_t *__restrict__ qw, int K, in
         const int g = (int)(bg % G);
         const int b = (int)(bg / G);
         const int gq = lane >> 2, tq = lane & 3;
-        const int r0 = (b * kBlockTiles + w) * kTileRows + gq, r1 = r0 + 8;
+        const int r0 = (b * kBlockTiles + w) * kTileRows + gq;
+        const int s0 = src_row(r0, N, swiglu_I), s1 = src_row(r0 + 8, N, swiglu_I);
         uint32_t res[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int kk = g * kGroup + c * kChunkK + 16 * tq + 4 * j;   // four k: kk .. kk+3
             const size_t wd = (size_t)kk / 8;                           // canonical word
             const int o = kk % 8;                                       // first nibble slot
-            const uint32_t a = r0 < N ? qw[r0 * words_per_row + wd] : 0u;
-            const uint32_t b = r1 < N ? qw[r1 * words_per_row + wd] : 0u;
+            const uint32_t a = s0 >= 0 ? qw[(size_t)s0 * words_per_row + wd] : 0u;
+            const uint32_t b = s1 >= 0 ? qw[(size_t)s1 * words_per_row + wd] : 0u;
             res[j] = nib(a, o) | (nib(b, o) << 4) | (nib(a, o + 2) << 8) |
                      (nib(b, o + 2) << 12) | (nib(a, o + 1) << 16) | (nib(b, o + 1) << 20) |
                      (nib(a, o + 3) << 24) | (nib(b, o + 3) << 28);
@@ -86,7 +103,8 @@ __global__ void repack_weights_kernel(const uint32_t *__restrict__ qw, int K, in
 }
 
 __global__ void repack_meta_kernel(const uint16_t *__restrict__ sc, const uint8_t *__restrict__ zp,
-                                   int K, int N, int NB, uint32_t *__restrict__ sc_out,
+                                   int K, int N, int NB, int swiglu_I,
+                                   uint32_t *__restrict__ sc_out,
                                    uint8_t *__restrict__ zp_out, Header *h) {
     const int G = K / kGroup;
     const size_t total = (size_t)NB * G * 64;
@@ -97,11 +115,12 @@ __global__ void repack_meta_kernel(const uint16_t *__restrict__ sc, const uint8_
         const size_t bg = i >> 6;
         const int g = (int)(bg % G);
         const int b = (int)(bg / G);
-        const int r0 = (b * kBlockTiles + w) * kTileRows + gq, r1 = r0 + 8;
-        const uint32_t s0 = r0 < N ? sc[(size_t)r0 * G + g] : 0u;
-        const uint32_t s1 = r1 < N ? sc[(size_t)r1 * G + g] : 0u;
-        const uint32_t z0 = r0 < N ? zp[(size_t)r0 * G + g] : 0u;
-        const uint32_t z1 = r1 < N ? zp[(size_t)r1 * G + g] : 0u;
+        const int r0 = (b * kBlockTiles + w) * kTileRows + gq;
+        const int c0 = src_row(r0, N, swiglu_I), c1 = src_row(r0 + 8, N, swiglu_I);
+        const uint32_t s0 = c0 >= 0 ? sc[(size_t)c0 * G + g] : 0u;
+        const uint32_t s1 = c1 >= 0 ? sc[(size_t)c1 * G + g] : 0u;
+        const uint32_t z0 = c0 >= 0 ? zp[(size_t)c0 * G + g] : 0u;
+        const uint32_t z1 = c1 >= 0 ? zp[(size_t)c1 * G + g] : 0u;
         if (z0 > 15u || z1 > 15u) atomicOr(&h->bad_zeros, 1u);
         sc_out[i] = s0 | (s1 << 16);
         zp_out[i] = (uint8_t)((z0 & 0xFu) | ((z1 & 0xFu) << 4));
@@ -117,19 +136,20 @@ int grid_for(size_t work, int threads) {
 }  // namespace
 
 cudaError_t launch_repack(const uint32_t *qweight, const uint16_t *scales, const uint8_t *zeros,
-                          int K, int N, void *qweight_out, void *scales_out, void *zeros_out,
-                          cudaStream_t stream) {
+                          int K, int N, int swiglu_I, void *qweight_out, void *scales_out,
+                          void *zeros_out, cudaStream_t stream) {
     const int NB = row_blocks(N);
     const int G = K / kGroup;
     Header *h = static_cast<Header *>(qweight_out);
-    write_header_kernel<<<1, 1, 0, stream>>>(h, K, N);
+    write_header_kernel<<<1, 1, 0, stream>>>(h, K, swiglu_I ? swiglu_I : N,
+                                             swiglu_I ? W4_LAYOUT_ID_SWIGLU : W4_LAYOUT_ID);
     const size_t pieces = (size_t)NB * G * (kRecWeights / 16);
     repack_weights_kernel<<<grid_for(pieces, 256), 256, 0, stream>>>(
-        qweight, K, N, NB,
+        qweight, K, N, NB, swiglu_I,
         reinterpret_cast<uint4 *>(static_cast<char *>(qweight_out) + W4_HEADER_BYTES));
     const size_t metas = (size_t)NB * G * 64;
     repack_meta_kernel<<<grid_for(metas, 256), 256, 0, stream>>>(
-        scales, zeros, K, N, NB, static_cast<uint32_t *>(scales_out),
+        scales, zeros, K, N, NB, swiglu_I, static_cast<uint32_t *>(scales_out),
         static_cast<uint8_t *>(zeros_out), h);
     return cudaGetLastError();
 }

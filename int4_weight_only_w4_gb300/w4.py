@@ -49,6 +49,13 @@ _check_header = _decl("w4_check_header", _ST, _P, _I, _I)
 _dequant = _decl("w4_dequant", _ST, _P, _P, _P, _I, _I, _P, _P)
 _gemv = _decl("w4_gemv", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_f32 = _decl("w4_gemv_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
+_repacked_sizes_swiglu = _decl("w4_repacked_sizes_swiglu", _ST, _I, _I,
+                               ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t),
+                               ctypes.POINTER(ctypes.c_size_t))
+_repack_swiglu = _decl("w4_repack_swiglu", _ST, _P, _P, _P, _I, _I, _P, _P, _P, _P)
+_check_header_swiglu = _decl("w4_check_header_swiglu", _ST, _P, _I, _I)
+_gemv_swiglu = _decl("w4_gemv_swiglu", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
+_gemv_swiglu_f32 = _decl("w4_gemv_swiglu_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _quantize = _decl("w4_quantize", _ST, _P, _I, _I, _I, _P, _P, _P, _P)
 _gemv_ws_static = _decl("w4_gemv_ws_static", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_config = _decl("w4_gemv_config", _ST, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
@@ -194,6 +201,39 @@ def gemv_ws_static(qweight, scales, zeros, x, y, M: int, K: int, N: int, stream=
                         _stream(stream, x)), "w4_gemv_ws_static")
 
 
+def repacked_sizes_swiglu(K: int, I: int):
+    """Byte sizes (qweight, scales, zeros) of the gate/up-interleaved layout."""
+    q, s, z = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _ok(_repacked_sizes_swiglu(K, I, ctypes.byref(q), ctypes.byref(s), ctypes.byref(z)),
+        "w4_repacked_sizes_swiglu")
+    return q.value, s.value, z.value
+
+
+def repack_swiglu(qweight, scales, zeros, K: int, I: int, qweight_out, scales_out, zeros_out,
+                  stream=None) -> None:
+    """w4_repack_swiglu: fused [2I, K] gate/up weight -> interleaved kernel layout."""
+    _ok(_repack_swiglu(_ptr(qweight), _ptr(scales), _ptr(zeros), K, I, _ptr(qweight_out),
+                       _ptr(scales_out), _ptr(zeros_out), _stream(stream, qweight)),
+        "w4_repack_swiglu")
+
+
+def check_header_swiglu(header_bytes: bytes, K: int, I: int) -> None:
+    buf = ctypes.create_string_buffer(bytes(header_bytes), HEADER_BYTES)
+    _ok(_check_header_swiglu(ctypes.cast(buf, ctypes.c_void_p), K, I), "w4_check_header_swiglu")
+
+
+def gemv_swiglu(qweight, scales, zeros, x, y, M: int, K: int, I: int, stream=None) -> None:
+    """w4_gemv_swiglu: y[M, I] (bfloat16) = silu(gate x) * (up x)."""
+    _ok(_gemv_swiglu(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, I,
+                     _stream(stream, x)), "w4_gemv_swiglu")
+
+
+def gemv_swiglu_f32(qweight, scales, zeros, x, y, M: int, K: int, I: int, stream=None) -> None:
+    """w4_gemv_swiglu_f32: the fp32 result."""
+    _ok(_gemv_swiglu_f32(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, I,
+                         _stream(stream, x)), "w4_gemv_swiglu_f32")
+
+
 QUANT_ASYMMETRIC = 0      # W4_QUANT_ASYMMETRIC
 QUANT_SYMMETRIC = 1       # W4_QUANT_SYMMETRIC
 
@@ -260,3 +300,42 @@ def pack(qweight: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor, K: in
     repack(qweight, scales, zeros, K, N, qo, so, zo, stream)
     check_header(qo[:HEADER_BYTES].cpu().numpy().tobytes(), K, N)
     return PackedWeight(K, N, qo, so, zo)
+
+
+@dataclass
+class PackedSwiGLU:
+    """A fused [2I, K] gate/up weight in the interleaved kernel layout."""
+    K: int
+    I: int
+    qweight: torch.Tensor
+    scales: torch.Tensor
+    zeros: torch.Tensor
+
+    def gemv(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """y[M, I] = silu(gate x) * (up x), bfloat16."""
+        M = x.shape[0]
+        if y is None:
+            y = torch.empty((M, self.I), dtype=torch.bfloat16, device=x.device)
+        gemv_swiglu(self.qweight, self.scales, self.zeros, x, y, M, self.K, self.I, stream)
+        return y
+
+    def gemv_f32(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None):
+        M = x.shape[0]
+        if y is None:
+            y = torch.empty((M, self.I), dtype=torch.float32, device=x.device)
+        gemv_swiglu_f32(self.qweight, self.scales, self.zeros, x, y, M, self.K, self.I, stream)
+        return y
+
+
+def pack_swiglu(qweight: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor, K: int,
+                I: int, stream=None) -> PackedSwiGLU:
+    """Allocate the interleaved-layout buffers (torch), repack the fused
+    [2I, K] gate/up weight into them and check the header once."""
+    dev = qweight.device
+    qb, sb, zb = repacked_sizes_swiglu(K, I)
+    qo = torch.empty(qb, dtype=torch.uint8, device=dev)
+    so = torch.empty(sb, dtype=torch.uint8, device=dev)
+    zo = torch.empty(zb, dtype=torch.uint8, device=dev)
+    repack_swiglu(qweight, scales, zeros, K, I, qo, so, zo, stream)
+    check_header_swiglu(qo[:HEADER_BYTES].cpu().numpy().tobytes(), K, I)
+    return PackedSwiGLU(K, I, qo, so, zo)
