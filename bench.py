@@ -547,6 +547,74 @@ def swiglu_arm(args):
     return 0
 
 
+GEMM_SHAPES = [("qwen7b.qkv", 3584, 4608), ("qwen7b.gate_up", 3584, 37888),
+               ("qwen7b.down", 18944, 3584)]
+GEMM_MS = (16, 32, 64, 128)
+
+
+def gemm_arm(args):
+    """Per-call timing of w4_gemm (passes of 8 tokens) for M > 8 on the 7B
+    layer shapes: R calls over rotating weight copies in one CUDA graph,
+    median of 5.  One JSON line per (shape, M): effective GB/s against the
+    algorithmic bytes (the weight once), and TFLOP/s (2 M N K)."""
+    import torch
+
+    from int4_weight_only_w4_gb300 import w4
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    peak, peak_kind = read_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    for name, K, N in GEMM_SHAPES:
+        qw, sc, zp = syn.make_weights(f"{name}.gemm", K, N, SEED, (0.001, 0.02))
+        base = w4.pack(torch.from_numpy(qw.view(np.int32)).to(dev),
+                       torch.from_numpy(sc.view(np.int16)).to(dev), torch.from_numpy(zp).to(dev),
+                       K, N)
+        qb, sb, zb = w4.repacked_sizes(K, N)
+        copies = min(64, max(2, -(-3 * l2 // (qb + sb + zb)) + 1))
+        packs = [base] + [w4.PackedWeight(K, N, base.qweight.clone(), base.scales.clone(),
+                                          base.zeros.clone()) for _ in range(copies - 1)]
+        for M in GEMM_MS:
+            x = torch.from_numpy(syn.make_x(f"{name}.gemm.M{M}", M, K, SEED).view(np.int16)) \
+                .to(dev).view(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            reps = max(2, copies)
+
+            def call(i):
+                pw = packs[i % copies]
+                w4.gemm(pw.qweight, pw.scales, pw.zeros, x, y, M, K, N, stream=stream)
+            with torch.cuda.stream(stream):
+                call(0)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(reps):
+                    call(i)
+            times = []
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    g.replay()
+                for _ in range(5):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                    e1.synchronize()
+                    times.append(e0.elapsed_time(e1) * 1e3 / reps)
+            us = statistics.median(times)
+            b = canonical_bytes(M, K, N)
+            print(json.dumps({"op": "w4_gemm", "shape": name, "M": M, "K": K, "N": N,
+                              "passes": -(-M // 8), "us_per_call": round(us, 3),
+                              "GBps": round(b / us / 1e3, 1),
+                              "frac_of_peak": round(b / us / 1e3 / peak, 4), "peak_kind": peak_kind,
+                              "TFLOPs": round(2.0 * M * N * K / us / 1e6, 2),
+                              "tok_per_s": round(M / us * 1e6, 1)}), flush=True)
+        del packs, base
+        torch.cuda.empty_cache()
+    return 0
+
+
 QUANT_SHAPES = [("qwen7b.gate_up", 3584, 37888), ("qwen7b.down", 18944, 3584),
                 ("qwen7b.lm_head", 3584, 152064)]
 
@@ -620,6 +688,8 @@ def main():
     ap.add_argument("--impl", choices=["w4", "reference"], default="w4")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm", action="store_true",
+                    help="per-call timing of w4_gemm (M > 8, passes of 8 tokens)")
     ap.add_argument("--swiglu", action="store_true",
                     help="per-call timing of the fused gate/up + SwiGLU product")
     ap.add_argument("--quantize", action="store_true",
@@ -637,6 +707,8 @@ def main():
         return quantize_arm(args)
     if args.swiglu:
         return swiglu_arm(args)
+    if args.gemm:
+        return gemm_arm(args)
     if args.per_shape or args.kernel_case:
         return per_shape_arm(args)
     return gpu_arm(args)

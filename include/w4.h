@@ -160,6 +160,24 @@ w4_status w4_gemv_f32(const void *qweight, const void *scales, const void *zeros
                       w4_stream_t stream);
 
 /*
+ * The product for any number of tokens M >= 1, in passes of at most 8 tokens
+ * over the same weight ("qengine", section "How the numbers were measured":
+ * prompts are processed in passes of 8 tokens): pass p is w4_gemv on tokens
+ * 8p .. 8p+7.  Row m of y is therefore bit-identical to w4_gemv on that
+ * token alone, for any M; the weight is streamed once per pass.
+ *   qweight, scales, zeros, x [M][K], y [M][N], stream : as for w4_gemv
+ * Errors: as w4_gemv, except that any M >= 1 is accepted (M < 1:
+ * W4_ERR_UNSUPPORTED); the passes are enqueued in order and the first error
+ * stops the rest.
+ */
+w4_status w4_gemm(const void *qweight, const void *scales, const void *zeros, const uint16_t *x,
+                  uint16_t *y, int M, int K, int N, w4_stream_t stream);
+
+/* w4_gemm writing the fp32 result before the bfloat16 cast (y: float [M][N]). */
+w4_status w4_gemm_f32(const void *qweight, const void *scales, const void *zeros,
+                      const uint16_t *x, float *y, int M, int K, int N, w4_stream_t stream);
+
+/*
  * Workspace for w4_gemv_ws on the current device, in bytes (depends on K, N
  * and the SM count only).  Errors: W4_ERR_INVALID_ARG, W4_ERR_CUDA (no device).
  */

@@ -76,6 +76,23 @@ w4_status check_header_common(const void *header, int K, int N, uint32_t layout_
     return W4_OK;
 }
 
+// Passes of at most 8 tokens over the same weight.
+w4_status gemm_common(const void *qweight, const void *scales, const void *zeros,
+                      const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
+                      w4_stream_t stream) {
+    if (M < 1) return W4_ERR_UNSUPPORTED;
+    if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
+    const size_t ybytes = f32_out ? 4 : 2;
+    for (int m0 = 0; m0 < M; m0 += W4_MAX_TOKENS) {
+        const int mp = M - m0 < W4_MAX_TOKENS ? M - m0 : W4_MAX_TOKENS;
+        const w4_status st = gemv_common(
+            qweight, scales, zeros, x + (size_t)m0 * K,
+            static_cast<char *>(y) + (size_t)m0 * N * ybytes, f32_out, mp, K, N, stream);
+        if (st != W4_OK) return st;
+    }
+    return W4_OK;
+}
+
 w4_status gemv_swiglu_common(const void *qweight, const void *scales, const void *zeros,
                              const uint16_t *x, void *y, bool f32_out, int M, int K, int I,
                              w4_stream_t stream) {
@@ -197,6 +214,16 @@ w4_status w4_gemv(const void *qweight, const void *scales, const void *zeros, co
 w4_status w4_gemv_f32(const void *qweight, const void *scales, const void *zeros,
                       const uint16_t *x, float *y, int M, int K, int N, w4_stream_t stream) {
     return gemv_common(qweight, scales, zeros, x, y, true, M, K, N, stream);
+}
+
+w4_status w4_gemm(const void *qweight, const void *scales, const void *zeros, const uint16_t *x,
+                  uint16_t *y, int M, int K, int N, w4_stream_t stream) {
+    return gemm_common(qweight, scales, zeros, x, y, false, M, K, N, stream);
+}
+
+w4_status w4_gemm_f32(const void *qweight, const void *scales, const void *zeros,
+                      const uint16_t *x, float *y, int M, int K, int N, w4_stream_t stream) {
+    return gemm_common(qweight, scales, zeros, x, y, true, M, K, N, stream);
 }
 
 w4_status w4_gemv_workspace_bytes(int K, int N, size_t *bytes) {

@@ -58,6 +58,8 @@ _gemv_swiglu = _decl("w4_gemv_swiglu", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_swiglu_f32 = _decl("w4_gemv_swiglu_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _quantize = _decl("w4_quantize", _ST, _P, _I, _I, _I, _P, _P, _P, _P)
 _gemv_ws_static = _decl("w4_gemv_ws_static", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
+_gemm = _decl("w4_gemm", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
+_gemm_f32 = _decl("w4_gemm_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_config = _decl("w4_gemv_config", _ST, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
                      ctypes.POINTER(_I))
 _gemv_workspace_bytes = _decl("w4_gemv_workspace_bytes", _ST, _I, _I,
@@ -155,6 +157,18 @@ def gemv_f32(qweight, scales, zeros, x, y, M: int, K: int, N: int, stream=None) 
     """w4_gemv_f32: as gemv but y is float32 (before the bfloat16 cast)."""
     _ok(_gemv_f32(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, N,
                   _stream(stream, x)), "w4_gemv_f32")
+
+
+def gemm(qweight, scales, zeros, x, y, M: int, K: int, N: int, stream=None) -> None:
+    """w4_gemm: y[M, N] (bfloat16) for any M >= 1, in passes of 8 tokens."""
+    _ok(_gemm(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, N,
+              _stream(stream, x)), "w4_gemm")
+
+
+def gemm_f32(qweight, scales, zeros, x, y, M: int, K: int, N: int, stream=None) -> None:
+    """w4_gemm_f32: as gemm, fp32 result."""
+    _ok(_gemm_f32(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, N,
+                  _stream(stream, x)), "w4_gemm_f32")
 
 
 def gemv_workspace_bytes(K: int, N: int) -> int:
