@@ -60,7 +60,7 @@ typedef enum w4_status {
 #define W4_MAX_TOKENS 8
 #define W4_LAYOUT_ID 1
 #define W4_LAYOUT_ID_SWIGLU 2      /* gate/up-interleaved layout (w4_repack_swiglu) */
-#define W4_LAYOUT_VERSION 3
+#define W4_LAYOUT_VERSION 4
 #define W4_HEADER_BYTES 128
 /* Size of the static device array behind w4_gemv_ws_static (4 MiB). */
 #define W4_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)

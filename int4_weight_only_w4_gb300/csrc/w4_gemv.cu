@@ -54,30 +54,31 @@ namespace {
 
 constexpr int kStageBytes = kRecWeights + kRecScales + kRecZeros;   // 8512
 constexpr int kStages = 6;                          // shared-memory ring depth
+constexpr int kStagesShort = 5;                     // ring depth that lets a third block fit
 constexpr size_t kBlockSmemBudget = 113 * 1024;     // two blocks per SM
-constexpr size_t kBlockSmemBudget3 = 74 * 1024;     // three blocks per SM (small M)
+constexpr size_t kBlockSmemBudget3 = 74 * 1024;     // three blocks per SM
 constexpr int kFoldMinGroups = 8;                   // see gemv_shape
 constexpr size_t kOverlapBelowBytes = 16u << 20;    // packed weights of a "short" product
 
 struct SmemPlan {
-    size_t x_off, x_row_bytes, zero_off, red_off, xsum_off, bar_off, total;
+    size_t x_off, x_row_bytes, red_off, xsum_off, tok_off, bar_off, total;
 };
 
 // Shared memory: [stages][weights | scales | zeros] [x rows as copied]
-// [one zero row when M < 8] [partials] [per-group sums of x] [barriers]
-__host__ __device__ inline SmemPlan smem_plan(int K, int S, int M) {
+// [partials] [per-group sums of x] [per-token maxima] [barriers]
+__host__ __device__ inline SmemPlan smem_plan(int K, int S, int M, int stages) {
     const int G = K / kGroup;
     const int gmax = (G + S - 1) / S;
     SmemPlan p;
-    p.x_off = (size_t)kStages * kStageBytes;
+    p.x_off = (size_t)stages * kStageBytes;
     p.x_row_bytes = (size_t)gmax * kGroup * 2 + 16;      // +16 B: rows land on other banks
-    p.zero_off = p.x_off + (size_t)M * p.x_row_bytes;
-    p.red_off = p.zero_off + (M < W4_MAX_TOKENS ? p.x_row_bytes : 0);
+    p.red_off = p.x_off + (size_t)M * p.x_row_bytes;
     // Receive slots for the tiles this block reduces: ceil(8 / S) tiles, one
     // 512-byte partial from each of the S blocks of the cluster.
     p.xsum_off = p.red_off + (S > 1 ? (size_t)S * ((kWarps + S - 1) / S) * 32 * 16 : 0);
-    p.bar_off = p.xsum_off + (size_t)gmax * W4_MAX_TOKENS * 4;   // float [gmax][8]
-    p.total = p.bar_off + (size_t)(2 * kStages + 1) * 8 + 8;   // + the two constants
+    p.tok_off = p.xsum_off + (size_t)gmax * 16 * 4;     // float [gmax][4 token pairs][4]
+    p.bar_off = p.tok_off + 64;                         // uint32 [8] (+ padding)
+    p.total = p.bar_off + (size_t)(2 * stages + 1) * 8 + 8;   // + the two constants
     return p;
 }
 
@@ -89,6 +90,16 @@ __host__ __device__ inline SmemPlan smem_plan(int K, int S, int M) {
 // partials visible, and each reducing warp adds its S slots from its own
 // shared memory.  No block reads another block's memory after the barrier,
 // so none has to wait for the others before exiting.
+// 2^e (or 2^-e for inverse) with e chosen so that 2^e times the bf16 value
+// whose magnitude bits are maxbits lies in [2^14, 2^15): the per-token scale
+// that brings x into fp16 range.  1 when the token's slice is all zero.
+__device__ __forceinline__ float token_scale(uint32_t maxbits, bool inverse) {
+    if (maxbits == 0) return 1.f;
+    int e = 141 - (int)(maxbits >> 7);                  // 14 - (bf16 exponent - 127)
+    e = e > 126 ? 126 : (e < -126 ? -126 : e);
+    return __uint_as_float((uint32_t)((inverse ? -e : e) + 127) << 23);
+}
+
 // Final store of a tile: y = W x, or the SwiGLU of the interleaved pairs.
 template <bool F32OUT>
 __device__ __forceinline__ void store_out(void *yv, const float (&acc)[4], int t, int lane, int M,
@@ -126,7 +137,7 @@ __device__ __forceinline__ void cluster_combine(float a0, float a1, float a2, fl
     }
 }
 
-template <bool F32OUT, int MIN_BLOCKS, bool FOLD>
+template <bool F32OUT, int MIN_BLOCKS, bool FOLD, int STAGES>
 __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
 gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             const char *__restrict__ zp, const __nv_bfloat16 *__restrict__ x,
@@ -141,7 +152,8 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
     const int g1 = (int)((long long)(split + 1) * G / S);
     const int ng = g1 - g0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const SmemPlan plan = smem_plan(K, S, M);
+    constexpr int kStages = STAGES;
+    const SmemPlan plan = smem_plan(K, S, M, kStages);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + plan.bar_off);
     uint64_t *empty = full + kStages;
     uint64_t *xbar = empty + kStages;
@@ -198,6 +210,7 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
                         if (base > 0 && !mbar_wait(&empty[i], phase ^ 1u)) {
                             ok = false;
                         } else {
+                            if (base > 0) fence_proxy_async();
                             unsigned char *st = smem + i * kStageBytes;
                             const size_t rec = (size_t)b * G + g0 + s;
                             mbar_expect_tx(&full[i], kStageBytes);
@@ -223,100 +236,167 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
     } else {
         // ---- consumers: warp w owns tile 8b + w ----
         const int gq = lane >> 2, tq = lane & 3;
-        // Token columns >= M read a row of zeros.
-        uint32_t *zrow = reinterpret_cast<uint32_t *>(smem + plan.zero_off);
         float *xsum = reinterpret_cast<float *>(smem + plan.xsum_off);
-        if (M < W4_MAX_TOKENS) {
-            for (int i = threadIdx.x; i < ng * 64; i += kWarps * 32) zrow[i] = 0u;
-            for (int i = threadIdx.x; i < ng * W4_MAX_TOKENS; i += kWarps * 32)
-                if ((i & (W4_MAX_TOKENS - 1)) >= M) xsum[i] = 0.f;
+        uint32_t *tok_max = reinterpret_cast<uint32_t *>(smem + plan.tok_off);
+        if (FOLD) {
+            // sums of tokens >= M stay zero; maxima start at zero
+            for (int i = threadIdx.x; i < ng * 16; i += kWarps * 32) xsum[i] = 0.f;
+            if (threadIdx.x < W4_MAX_TOKENS) tok_max[threadIdx.x] = 0u;
+            consumer_sync();
         }
-        consumer_sync();
         // x is used as copied: the kernel layout orders k inside each 64-k chunk
         // so that lane tq's eight B registers are the x pairs at
         // 64c + 16tq .. 64c + 16tq + 15 (see w4_repack.cu).
+        // Token columns gq >= M read token 0's row: column n of a tensor-core
+        // product depends on column n of B alone, and those columns are never
+        // stored.
         const uint32_t *xrow =
-            (gq < M ? reinterpret_cast<const uint32_t *>(xs + (size_t)gq * plan.x_row_bytes)
-                    : zrow) + tq * 8;    // words 8tq .. 8tq+7 of each 32-word chunk
+            reinterpret_cast<const uint32_t *>(xs + (size_t)(gq < M ? gq : 0) * plan.x_row_bytes) +
+            tq * 8;    // words 8tq .. 8tq+7 of each 32-word chunk
         const float zq[4] = {0.f, 0.f, 0.f, 0.f};
-        // The two conversion constants, read from shared memory so that they
-        // sit in ordinary registers: left as kernel parameters, the compiler
-        // may keep them in uniform registers, and a three-input logic
-        // operation takes only one of those, which costs a register move per
-        // extraction.
+        // The conversion constants, read from shared memory so that they sit
+        // in ordinary registers: left as kernel parameters, the compiler may
+        // keep them in uniform registers, and a three-input logic operation
+        // takes only one of those, which costs a register move per extraction.
         const uint32_t mask = reinterpret_cast<volatile uint32_t *>(xbar + 1)[0];
         const uint32_t magic = reinterpret_cast<volatile uint32_t *>(xbar + 1)[1];
+        const uint32_t mask_hi = mask << 4;
         // Sleep (no polling) until the previous kernel in the stream is done:
         // x may be its output, and a block launched early must not take issue
         // slots from that kernel's still-running blocks.
         wait_prerequisites();
         {
-            // Per group and token, the sum of the group's 128 x values, for the
-            // zero-point term of group_mma_folded.  The fp32 arithmetic is
-            // fixed: eight partial sums of 16 consecutive values (left to
-            // right), then the pairwise tree ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)).
-            // Only the assignment of that work to threads depends on the
-            // number of (group, token) pairs: tpp threads per pair, each with
-            // 8 / tpp partials, joined by shuffles that follow the same tree.
-            // Every consumer thread takes part in the barrier below even if
+            // Every consumer thread takes part in the barriers below even if
             // its wait gave up.
             const bool x_ok = mbar_wait(xbar, 0);
-            if (FOLD && x_ok) {
-                const int pairs = ng * M;
-                int tpp = 8;
-                while (tpp > 1 && pairs * tpp > kWarps * 32) tpp >>= 1;
-                const int per = 8 / tpp;
-                for (int base = 0; base < pairs * tpp; base += kWarps * 32) {
-                    const int idx = base + (int)threadIdx.x;
-                    const int pair = idx / tpp, sub = idx - pair * tpp;
-                    float part[8];
-                    if (pair < pairs) {
-                        const int gl = pair / M, m = pair - gl * M;
-                        const uint4 *src = reinterpret_cast<const uint4 *>(
-                            xs + (size_t)m * plan.x_row_bytes + (size_t)gl * kGroup * 2 +
-                            (size_t)sub * per * 32);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            if (j < per) {
-                                const uint4 u0 = src[2 * j], u1 = src[2 * j + 1];
-                                const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w,
-                                                       u1.x, u1.y, u1.z, u1.w};
-                                float acc_j = __uint_as_float(w[0] << 16);
-#pragma unroll
-                                for (int e = 1; e < 16; ++e)
-                                    acc_j += __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u)
-                                                                     : (w[e >> 1] << 16));
-                                part[j] = acc_j;
-                            }
+            if constexpr (FOLD) {
+                // The folded product runs on fp16 operands: x is scaled per
+                // token by a power of two (exact) into fp16 range.  (1) The
+                // largest |x| of each token's slice, as bf16 magnitude bits
+                // (whose integer order is the order of the values).
+                if (x_ok) {
+                    for (int m = 0; m < M; ++m) {
+                        const uint4 *row =
+                            reinterpret_cast<const uint4 *>(xs + (size_t)m * plan.x_row_bytes);
+                        uint32_t mx2 = 0u;              // two 16-bit maxima
+                        for (int i = threadIdx.x; i < ng * 16; i += kWarps * 32) {
+                            const uint4 v = row[i];
+                            mx2 = __vmaxu2(mx2, v.x & 0x7FFF7FFFu);
+                            mx2 = __vmaxu2(mx2, v.y & 0x7FFF7FFFu);
+                            mx2 = __vmaxu2(mx2, v.z & 0x7FFF7FFFu);
+                            mx2 = __vmaxu2(mx2, v.w & 0x7FFF7FFFu);
                         }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) part[j] = 0.f;
-                    }
-                    // this thread's subtree over its `per` partials
-                    if (per >= 2) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (2 * j + 1 < per) part[2 * j] = part[2 * j] + part[2 * j + 1];
-                    }
-                    if (per >= 4) {
-                        part[0] = part[0] + part[2];
-                        if (per == 8) part[4] = part[4] + part[6];
-                    }
-                    if (per == 8) part[0] = part[0] + part[4];
-                    float v = part[0];
-                    for (int o = 1; o < tpp; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                    if (sub == 0 && pair < pairs) {
-                        const int gl = pair / M, m = pair - gl * M;
-                        xsum[gl * W4_MAX_TOKENS + m] = v;
+                        const uint32_t mx =
+                            __reduce_max_sync(0xFFFFFFFFu, max(mx2 & 0xFFFFu, mx2 >> 16));
+                        if (lane == 0 && mx) atomicMax(&tok_max[m], mx);
                     }
                 }
+                consumer_sync();
+                // (2) x -> fp16 (scaled, rounded to nearest), in place, and per
+                // group and token the two sums X01 (k mod 16 < 8) and X23
+                // (k mod 16 >= 8) of the scaled values for the zero-point term
+                // of group_mma_half_folded (the fp16 values equal them except
+                // below the fp16 normal range, 2^28 under the token's largest).
+                // The fp32 arithmetic is fixed: per 16-aligned block of the
+                // group and half (first or last eight values), the values at
+                // even and at odd positions are summed left to right in two
+                // packed lanes and the two lane sums added; then over the
+                // eight blocks the pairwise tree ((p0+p1)+(p2+p3))+((p4+p5)+
+                // (p6+p7)).  Only the assignment of that work to threads
+                // depends on the number of (group, token) pairs: tpp threads
+                // per pair, each with 8 / tpp blocks, joined by shuffles that
+                // follow the same tree.
+                if (x_ok) {
+                    const int pairs = ng * M;
+                    int tpp = 8;
+                    while (tpp > 1 && pairs * tpp > kWarps * 32) tpp >>= 1;
+                    const int per = 8 / tpp;
+                    for (int base = 0; base < pairs * tpp; base += kWarps * 32) {
+                        const int idx = base + (int)threadIdx.x;
+                        const int pair = idx / tpp, sub = idx - pair * tpp;
+                        const int gl = pair / M, m = pair - gl * M;
+                        float p01[8], p23[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) p01[j] = p23[j] = 0.f;
+                        if (pair < pairs) {
+                            const float sc = token_scale(tok_max[m], false);
+                            const unsigned long long sc2 =
+                                ((unsigned long long)__float_as_uint(sc) << 32) | __float_as_uint(sc);
+                            uint4 *blk = reinterpret_cast<uint4 *>(
+                                xs + (size_t)m * plan.x_row_bytes + (size_t)gl * kGroup * 2 +
+                                (size_t)sub * per * 32);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                if (j < per) {
+                                    const uint4 u0 = blk[2 * j], u1 = blk[2 * j + 1];
+                                    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w,
+                                                           u1.x, u1.y, u1.z, u1.w};
+                                    uint32_t h[8];
+                                    unsigned long long a01 = 0ull, a23 = 0ull;
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        // the pair as fp32 (bf16 is the top half of fp32),
+                                        // scaled
+                                        const unsigned long long f = f32x2_mul(
+                                            ((unsigned long long)(w[e] & 0xFFFF0000u) << 32) |
+                                                (unsigned long long)(w[e] << 16),
+                                            sc2);
+                                        const __half2 v = __floats2half2_rn(f32x2_lo(f), f32x2_hi(f));
+                                        h[e] = *reinterpret_cast<const uint32_t *>(&v);
+                                        if (e < 4)
+                                            a01 = e == 0 ? f : f32x2_add(a01, f);
+                                        else
+                                            a23 = e == 4 ? f : f32x2_add(a23, f);
+                                    }
+                                    blk[2 * j] = make_uint4(h[0], h[1], h[2], h[3]);
+                                    blk[2 * j + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+                                    p01[j] = f32x2_lo(a01) + f32x2_hi(a01);
+                                    p23[j] = f32x2_lo(a23) + f32x2_hi(a23);
+                                }
+                            }
+                        }
+                        // this thread's subtree over its `per` blocks, then the
+                        // shuffles over the pair's tpp threads
+                        if (per >= 2) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                if (2 * j + 1 < per) {
+                                    p01[2 * j] = p01[2 * j] + p01[2 * j + 1];
+                                    p23[2 * j] = p23[2 * j] + p23[2 * j + 1];
+                                }
+                            }
+                        }
+                        if (per >= 4) {
+                            p01[0] = p01[0] + p01[2];
+                            p23[0] = p23[0] + p23[2];
+                            if (per == 8) {
+                                p01[4] = p01[4] + p01[6];
+                                p23[4] = p23[4] + p23[6];
+                            }
+                        }
+                        if (per == 8) {
+                            p01[0] = p01[0] + p01[4];
+                            p23[0] = p23[0] + p23[4];
+                        }
+                        float v01 = p01[0], v23 = p23[0];
+                        for (int o = 1; o < tpp; o <<= 1) {
+                            v01 += __shfl_xor_sync(0xFFFFFFFFu, v01, o);
+                            v23 += __shfl_xor_sync(0xFFFFFFFFu, v23, o);
+                        }
+                        if (sub == 0 && pair < pairs) {
+                            float *xg = xsum + gl * 16 + (m >> 1) * 4 + (m & 1);
+                            xg[0] = v01;
+                            xg[2] = v23;
+                        }
+                    }
+                }
+                consumer_sync();
             }
-            if constexpr (FOLD) consumer_sync();
             if (!x_ok) goto consumer_failed;
         }
         {
-            const float2 *xs2 = reinterpret_cast<const float2 *>(xsum) + tq;
+            // (X01, X01, X23, X23) of tokens 2tq, 2tq+1 for each group
+            const float4 *xs4 = reinterpret_cast<const float4 *>(xsum) + tq;
             uint32_t phase = 0;                 // round of the ring, mod 2
             int s = 0;
             for (; s + kStages <= ng; s += kStages) {
@@ -327,8 +407,8 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[i]);   // stage copied to registers
                     if constexpr (FOLD)
-                        group_mma_folded(acc, g, load_b(xrow + (s + i) * 64), xs2[(s + i) * 4],
-                                         zq, mask, magic);
+                        group_mma_half_folded(acc, g, load_b(xrow + (s + i) * 64),
+                                              xs4[(s + i) * 4], zq, mask, mask_hi, magic);
                     else
                         group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, mask, magic);
                 }
@@ -342,12 +422,22 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[i]);
                     if constexpr (FOLD)
-                        group_mma_folded(acc, g, load_b(xrow + (s + i) * 64), xs2[(s + i) * 4],
-                                         zq, mask, magic);
+                        group_mma_half_folded(acc, g, load_b(xrow + (s + i) * 64),
+                                              xs4[(s + i) * 4], zq, mask, mask_hi, magic);
                     else
                         group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, mask, magic);
                 }
             }
+        }
+        if constexpr (FOLD) {
+            // undo the per-token scale of x (a power of two: exact)
+            const int m0 = 2 * tq, m1 = m0 + 1;
+            const float u0 = m0 < M ? token_scale(tok_max[m0], true) : 1.f;
+            const float u1 = m1 < M ? token_scale(tok_max[m1], true) : 1.f;
+            acc[0] *= u0;
+            acc[1] *= u1;
+            acc[2] *= u0;
+            acc[3] *= u1;
         }
         goto consumer_done;
     consumer_failed:
@@ -380,7 +470,7 @@ bool gemv_shape(int K, int N, int num_sms, GemvShape *out) {
     long long best_cost = 0;
     for (int S : kCandidates) {
         if (S > G || S > kMaxSplits) continue;
-        if (smem_plan(K, S, W4_MAX_TOKENS).total > kBlockSmemBudget) continue;
+        if (smem_plan(K, S, W4_MAX_TOKENS, kStages).total > kBlockSmemBudget) continue;
         const long long ctas = (long long)NB * S;
         // A clustered grid counts as one wave only with 10% of the slots to
         // spare, as in launch_gemv (beyond that it runs uncapped and slower).
@@ -451,11 +541,17 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
                         const GemvShape &shape, int swiglu_I, int num_sms,
                         cudaStream_t stream) {
     const int S = shape.splits;
-    // Small M: x is small, so three blocks fit per SM (more warps to hide
-    // latency).  The split S, and so the arithmetic, is the same either way.
-    const SmemPlan plan = smem_plan(K, S, M);
-    const bool three = M <= 2 && plan.total <= kBlockSmemBudget3;
-    static bool attr_done[2][2][2][64] = {};
+    // Residency: three blocks per SM (more warps to hide the prologue and
+    // memory latency) where x's slice leaves room for them, with a ring of
+    // six stages or else five; otherwise two blocks with six.  The split S,
+    // and so the arithmetic, is the same whichever runs.
+    int variant = 0;                    // 0: two blocks, 6 stages; 1: three, 6; 2: three, 5
+    if (smem_plan(K, S, M, kStages).total <= kBlockSmemBudget3)
+        variant = 1;
+    else if (smem_plan(K, S, M, kStagesShort).total <= kBlockSmemBudget3)
+        variant = 2;
+    const SmemPlan plan = smem_plan(K, S, M, variant == 2 ? kStagesShort : kStages);
+    static bool attr_done[2][3][2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -464,16 +560,18 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     using Kern = void (*)(const char *, const char *, const char *, const __nv_bfloat16 *,
                           void *, uint32_t *, int, int, int, int, int, int, uint32_t,
                           uint32_t);
-    static const Kern kKernels[2][2][2] = {
-        {{gemv_kernel<false, 2, false>, gemv_kernel<false, 2, true>},
-         {gemv_kernel<false, 3, false>, gemv_kernel<false, 3, true>}},
-        {{gemv_kernel<true, 2, false>, gemv_kernel<true, 2, true>},
-         {gemv_kernel<true, 3, false>, gemv_kernel<true, 3, true>}}};
-    const Kern kern = kKernels[f32_out][three][shape.fold];
-    if (!attr_done[f32_out][three][shape.fold][dev]) {
+    static const Kern kKernels[2][3][2] = {
+        {{gemv_kernel<false, 2, false, kStages>, gemv_kernel<false, 2, true, kStages>},
+         {gemv_kernel<false, 3, false, kStages>, gemv_kernel<false, 3, true, kStages>},
+         {gemv_kernel<false, 3, false, kStagesShort>, gemv_kernel<false, 3, true, kStagesShort>}},
+        {{gemv_kernel<true, 2, false, kStages>, gemv_kernel<true, 2, true, kStages>},
+         {gemv_kernel<true, 3, false, kStages>, gemv_kernel<true, 3, true, kStages>},
+         {gemv_kernel<true, 3, false, kStagesShort>, gemv_kernel<true, 3, true, kStagesShort>}}};
+    const Kern kern = kKernels[f32_out][variant][shape.fold];
+    if (!attr_done[f32_out][variant][shape.fold][dev]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ds.optin);
         if (e != cudaSuccess) return e;
-        attr_done[f32_out][three][shape.fold][dev] = true;
+        attr_done[f32_out][variant][shape.fold][dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)row_blocks(N), (unsigned)S, 1);
@@ -533,7 +631,8 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     return cudaLaunchKernelEx(&cfg, kern, q, static_cast<const char *>(scales),
                               static_cast<const char *>(zeros),
                               reinterpret_cast<const __nv_bfloat16 *>(x), y, err, M, K, N, S,
-                              overlap ? 2 : 0, swiglu_I, 0x000F000Fu, 0x43004300u);
+                              overlap ? 2 : 0, swiglu_I, 0x000F000Fu,
+                              shape.fold ? 0x64006400u : 0x43004300u);
 }
 
 }  // namespace w4

@@ -183,6 +183,7 @@ gemv_sk_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
                     ok = false;
                     break;
                 }
+                if (s >= kSkStages) fence_proxy_async();
                 unsigned char *st = smem + i * kSkStageBytes;
                 mbar_expect_tx(&full[i], stage_tx);
                 bulk_g2s(st, qp, kRecWeights, &full[i]);

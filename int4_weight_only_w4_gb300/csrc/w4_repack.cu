@@ -8,26 +8,32 @@
 // group g -- holds, in each of the three buffers:
 //   qweight: 8 KB at 128 + (b*G + g) * 8192: tile w (0..7), chunk c (0..1,
 //            64 k each, kc = 128g + 64c), lane l = 4*gq + tq: 16 bytes at
-//            w*1024 + c*512 + l*16, four 32-bit words, one per k-step j = 0..3
-//            of the tensor-core operation.  The sum over k does not depend on
-//            the order of k, so inside a chunk the k-steps take a permuted k:
-//            column pair (2tq, 2tq+1) of step j is k = kc + 16tq + 4j + {0, 1}
-//            and column pair (2tq+8, 2tq+9) is k = kc + 16tq + 4j + {2, 3}.
-//            With that order the B registers a lane needs for the chunk are
-//            the eight consecutive x pairs starting at kc + 16tq: two 16-byte
-//            loads straight from x as copied, no rearranging.  Word j holds
-//            the eight nibbles the lane owns in the A fragment of step j,
-//            arranged so that (word >> 4p) & 0x000F000F gives A register p as
-//            a pair (low half: the first k of the pair, high half: the second):
-//              bits  0- 3 / 16-19 : row 16t+gq,   k = kk+0 / kk+1   (reg 0)
-//              bits  4- 7 / 20-23 : row 16t+gq+8, k = kk+0 / kk+1   (reg 1)
-//              bits  8-11 / 24-27 : row 16t+gq,   k = kk+2 / kk+3   (reg 2)
-//              bits 12-15 / 28-31 : row 16t+gq+8, k = kk+2 / kk+3   (reg 3)
-//            with t = 8b + w and kk = kc + 16tq + 4j.  This is the even/odd
-//            pair interleave of "Building an LLM Inference Runtime ...",
-//            section "Bug #3" (nibble slots hold w0,w2,w4,w6 in the low
-//            half-word and w1,w3,w5,w7 in the high one), extended to the two
-//            rows of a fragment.
+//            w*1024 + c*512 + l*16, four 32-bit words v = 0..3.  The sum over
+//            k does not depend on the order of k, so inside a chunk the four
+//            k-steps j of the tensor-core operation take a permuted k: column
+//            pair (2tq, 2tq+1) of step j is k = kc + 16tq + 4j + {0, 1} and
+//            column pair (2tq+8, 2tq+9) is k = kc + 16tq + 4j + {2, 3}.  With
+//            that order the B registers a lane needs for the chunk are the
+//            eight consecutive x pairs starting at kc + 16tq: two 16-byte loads
+//            straight from x as copied, no rearranging.  With
+//            k0 = kc + 16tq + 4*(v >> 1) + 2*(v & 1), word v holds the pairs
+//            (first k of a pair in the low half-word, second in the high one):
+//              bits  0- 3 / 16-19 : row 16t+gq,   k = k0     / k0 + 1
+//              bits  4- 7 / 20-23 : row 16t+gq,   k = k0 + 8 / k0 + 9
+//              bits  8-11 / 24-27 : row 16t+gq+8, k = k0     / k0 + 1
+//              bits 12-15 / 28-31 : row 16t+gq+8, k = k0 + 8 / k0 + 9
+//            with t = 8b + w.  Steps 0 and 1 of the chunk take their A
+//            registers from the nibbles at bits 0-3 and 8-11 of words
+//            (0, 1) and (2, 3); steps 2 and 3 from bits 4-7 and 12-15.  So
+//            word & 0x000F000F, word & 0x00F000F0, (word >> 8) & 0x000F000F
+//            and (word >> 8) & 0x00F000F0 are A registers as they stand: one
+//            shift per word (the second pair of each half-word sits four bits
+//            higher, which an fp16 mantissa absorbs as a factor 16; see
+//            w4_device.cuh).  This is the even/odd pair interleave of
+//            "Building an LLM Inference Runtime ...", section "Bug #3"
+//            (nibble slots hold w0,w2,w4,w6 in the low half-word and
+//            w1,w3,w5,w7 in the high one), extended to the two rows and the
+//            two step pairs of a fragment.
 //   scales:  256 B at (b*G + g) * 256: uint32 [w][gq] = fp16 scale of row
 //            16t+gq (low half) and of row 16t+gq+8 (high half).
 //   zeros:   64 B at (b*G + g) * 64: byte [w][gq] = z of row 16t+gq (low
@@ -86,17 +92,19 @@ __global__ void repack_weights_kernel(const uint32_t *__restrict__ qw, int K, in
         const int gq = lane >> 2, tq = lane & 3;
         const int r0 = (b * kBlockTiles + w) * kTileRows + gq;
         const int s0 = src_row(r0, N, swiglu_I), s1 = src_row(r0 + 8, N, swiglu_I);
+        const uint32_t *ra = s0 >= 0 ? qw + (size_t)s0 * words_per_row : nullptr;
+        const uint32_t *rb = s1 >= 0 ? qw + (size_t)s1 * words_per_row : nullptr;
+        // nibble of canonical row r (base pointer) at k; 0 for a zero row
+        auto q = [](const uint32_t *r, int k) -> uint32_t {
+            return r ? nib(r[k / 8], k % 8) : 0u;
+        };
         uint32_t res[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int kk = g * kGroup + c * kChunkK + 16 * tq + 4 * j;   // four k: kk .. kk+3
-            const size_t wd = (size_t)kk / 8;                           // canonical word
-            const int o = kk % 8;                                       // first nibble slot
-            const uint32_t a = s0 >= 0 ? qw[(size_t)s0 * words_per_row + wd] : 0u;
-            const uint32_t b = s1 >= 0 ? qw[(size_t)s1 * words_per_row + wd] : 0u;
-            res[j] = nib(a, o) | (nib(b, o) << 4) | (nib(a, o + 2) << 8) |
-                     (nib(b, o + 2) << 12) | (nib(a, o + 1) << 16) | (nib(b, o + 1) << 20) |
-                     (nib(a, o + 3) << 24) | (nib(b, o + 3) << 28);
+        for (int v = 0; v < 4; ++v) {
+            const int k0 = g * kGroup + c * kChunkK + 16 * tq + 4 * (v >> 1) + 2 * (v & 1);
+            res[v] = q(ra, k0) | (q(ra, k0 + 8) << 4) | (q(rb, k0) << 8) | (q(rb, k0 + 8) << 12) |
+                     (q(ra, k0 + 1) << 16) | (q(ra, k0 + 9) << 20) | (q(rb, k0 + 1) << 24) |
+                     (q(rb, k0 + 9) << 28);
         }
         out[i] = make_uint4(res[0], res[1], res[2], res[3]);
     }

@@ -111,7 +111,7 @@ def test_dequant_and_repack_argument_errors(lib):
     assert lib.w4_repack(FAKE, FAKE, FAKE, 64, 4, FAKE, FAKE, FAKE, None) == 1
 
 
-def header(K, N, magic=b"W4G128KL", layout=1, version=3, bad=0, kerr=0):
+def header(K, N, magic=b"W4G128KL", layout=1, version=4, bad=0, kerr=0):
     return magic + struct.pack("<IIiiII", layout, version, K, N, bad, kerr) + bytes(96)
 
 

@@ -16,14 +16,19 @@ def test_folded_abs_matches_brute_force_and_dominates():
     for m in range(M):
         for n in (0, 7, N - 1):
             tot = 0.0
+            wsum = 0.0
             for g in range(K // 128):
                 acc = 0.0
+                z = int(p.zeros[n, g])
                 for k in range(g * 128, g * 128 + 128):
                     q = (int(p.qweight[n, k // 8]) >> (4 * (k % 8))) & 0xF
-                    acc += (128 + q) * abs(x[m, k])
-                acc += (128 + int(p.zeros[n, g])) * np.abs(x[m, g * 128:g * 128 + 128]).sum()
+                    first_half = (k % 16) < 8
+                    acc += ((1024 if first_half else 64) + q) * abs(x[m, k])
+                    acc += ((1024 if first_half else 64) + z) * abs(x[m, k])
+                    wsum += abs(s[n, g]) * ((1024 if first_half else 64) + q)
                 tot += abs(s[n, g]) * acc
+            tot += wsum * max(np.abs(x[m]).max() * 2.0 ** -39, 2.0 ** -151) / 2.0 ** -23
             assert np.isclose(got[m, n], tot, rtol=1e-12)
-    # (128 + q) >= |q - z|: the folded magnitudes bound the plain ones
+    # (64 + q) >= |q - z|: the folded magnitudes bound the plain ones
     _, refabs = oracle.gemv_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N, with_abs=True)
     assert (got >= refabs).all()

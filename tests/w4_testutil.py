@@ -13,9 +13,15 @@ splits + 1, and A the sum of the magnitudes of the terms that are actually
 rounded:
   * exact zero-point subtraction (A = q - z in the tensor-core operand, the
     workspace split): A = sum_k |w_k x_k| (the oracle's `with_abs` sum);
-  * zero point folded out of the inner product (the cluster split computes
-    sum (128 + q) x - (128 + z) sum x per group): A = folded_abs(), and n
-    grows by 8 for the group sums of x (a 7-level tree, then one fma).
+  * zero point folded out of the inner product (the cluster split, fp16
+    operands: per group d0 = sum over S01 of (1024 + q) x and d1 / 16 = sum
+    over S23 of (64 + q) x, minus (1024 + z) X01 and (64 + z) X23, where
+    S01 = {k : k mod 16 < 8}, S23 the rest, X the sums of x over them):
+    A = folded_abs(), and n grows by 8 for the group sums (a tree of at most
+    7 levels, then the fma).  x enters as fp16 scaled per token by a power of
+    two into [2^14, 2^15): exact except for values more than 2^28 below the
+    token's largest, whose rounding (at most 2^-39 times that largest value
+    each) the bound also covers.
 """
 from __future__ import annotations
 
@@ -60,8 +66,14 @@ def _bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 def folded_abs(p, rows=None) -> np.ndarray:
-    """Per output [M, len(rows)]: sum over groups g of |s_g| * (sum_k (128 + q_k)|x_k|
-    + (128 + z_g) sum_k |x_k|), the magnitudes rounded by the folded arithmetic."""
+    """Per output [M, len(rows)]: sum over groups g of |s_g| * (sum_{S01} (1024 + q)|x|
+    + sum_{S23} (64 + q)|x| + (1024 + z) sum_{S01} |x| + (64 + z) sum_{S23} |x|),
+    the magnitudes rounded by the folded arithmetic, plus the fp16 rounding of
+    tiny x, in units of the bound's u = 2^-23.  The tensor-core product sees
+    the fp16 value x16 and the zero-point term the fp32 sum of the scaled x,
+    so each weight adds |s| (1024 + q or 64 + q) |x16 - x|: at most half an
+    fp16 subnormal step, 2^-25, over the token's scale 2^e, which is at most
+    2^-39 max |x| (2^e max |x| >= 2^14), or 2^-151 where e is clamped."""
     rows = np.arange(p.N) if rows is None else np.asarray(rows)
     K, M = p.K, p.M
     G = K // 128
@@ -72,11 +84,15 @@ def folded_abs(p, rows=None) -> np.ndarray:
     s = np.abs(np.asarray(p.scales)[rows].view(np.float16).astype(np.float64))   # [R, G]
     z = np.asarray(p.zeros)[rows].astype(np.float64)                              # [R, G]
     xa = np.abs(_bf16_to_f64(p.x)).reshape(M, G, 128)                             # [M, G, 128]
-    a = (128.0 + q).reshape(len(rows), G, 128)
+    lo = (np.arange(128) % 16) < 8                                                # S01
+    a = np.where(lo[None, None, :], 1024.0, 64.0) + q.reshape(len(rows), G, 128)
     out = np.empty((M, len(rows)))
     for m in range(M):
-        t = np.einsum("rgk,gk->rg", a, xa[m]) + (128.0 + z) * xa[m].sum(-1)[None, :]
-        out[m] = (s * t).sum(-1)
+        t = np.einsum("rgk,gk->rg", a, xa[m]) + (1024.0 + z) * xa[m][:, lo].sum(-1)[None, :] \
+            + (64.0 + z) * xa[m][:, ~lo].sum(-1)[None, :]
+        tiny = (a * s[:, :, None]).sum((1, 2)) * max(xa[m].max() * 2.0 ** -39, 2.0 ** -151) \
+            / 2.0 ** -23
+        out[m] = (s * t).sum(-1) + tiny
     return out
 
 
