@@ -59,6 +59,7 @@ constexpr size_t kBlockSmemBudget = 113 * 1024;     // two blocks per SM
 constexpr size_t kBlockSmemBudget3 = 74 * 1024;     // three blocks per SM
 constexpr int kFoldMinGroups = 8;                   // see gemv_shape
 constexpr size_t kOverlapBelowBytes = 16u << 20;    // packed weights of a "short" product
+constexpr int kPersistMinTokens = 3;                // see launch_gemv
 
 struct SmemPlan {
     size_t x_off, x_row_bytes, red_off, xsum_off, tok_off, bar_off, total;
@@ -137,7 +138,10 @@ __device__ __forceinline__ void cluster_combine(float a0, float a1, float a2, fl
     }
 }
 
-template <bool F32OUT, int MIN_BLOCKS, bool FOLD, int STAGES>
+// PERSIST (split S = 1 only): block c takes row blocks c, c + gridDim.x, ...
+// in turn through one ring and one x prologue; otherwise block (b, split)
+// takes row block b's K slice `split`.
+template <bool F32OUT, int MIN_BLOCKS, bool FOLD, int STAGES, bool PERSIST>
 __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
 gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             const char *__restrict__ zp, const __nv_bfloat16 *__restrict__ x,
@@ -151,6 +155,9 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
     const int g0 = (int)((long long)split * G / S);
     const int g1 = (int)((long long)(split + 1) * G / S);
     const int ng = g1 - g0;
+    // units (row block, group) this block streams, row block by row block
+    const int nrb = PERSIST ? (row_blocks(N) - b + (int)gridDim.x - 1) / (int)gridDim.x : 1;
+    const int U = nrb * ng;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int kStages = STAGES;
     const SmemPlan plan = smem_plan(K, S, M, kStages);
@@ -185,10 +192,15 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             // first), then the rest.  Launched normally (pre = 0), the wait
             // returns at once and x goes ahead of every weight copy.
             int issued = 0;
-            const int first = ng < pre ? ng : pre;  // < kStages: no ring waits needed
+            int pb = b, ps = 0;                     // row block and group of the next unit
+            const int first = U < pre ? U : pre;    // < kStages: no ring waits needed
             for (int s = 0; s < first; ++s) {
                 unsigned char *st = smem + s * kStageBytes;
-                const size_t rec = (size_t)b * G + g0 + s;
+                const size_t rec = PERSIST ? (size_t)pb * G + g0 + ps : (size_t)b * G + g0 + s;
+                if (PERSIST && ++ps == ng) {
+                    ps = 0;
+                    pb += (int)gridDim.x;
+                }
                 mbar_expect_tx(&full[s], kStageBytes);
                 bulk_g2s(st, qw + W4_HEADER_BYTES + rec * kRecWeights, kRecWeights, &full[s]);
                 bulk_g2s(st + kRecWeights, sc + rec * kRecScales, kRecScales, &full[s]);
@@ -202,17 +214,22 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
                 bulk_g2s(xs + m * plan.x_row_bytes, x + (size_t)m * K + (size_t)g0 * kGroup,
                          (uint32_t)(ng * kGroup * 2), xbar);
             uint32_t phase = 0;                     // round of the ring, mod 2
-            for (int base = 0; base < ng && ok; base += kStages) {
+            for (int base = 0; base < U && ok; base += kStages) {
 #pragma unroll
                 for (int i = 0; i < kStages; ++i) {
                     const int s = base + i;
-                    if (s >= first && s < ng && ok) {
+                    if (s >= first && s < U && ok) {
                         if (base > 0 && !mbar_wait(&empty[i], phase ^ 1u)) {
                             ok = false;
                         } else {
                             if (base > 0) fence_proxy_async();
                             unsigned char *st = smem + i * kStageBytes;
-                            const size_t rec = (size_t)b * G + g0 + s;
+                            const size_t rec =
+                                PERSIST ? (size_t)pb * G + g0 + ps : (size_t)b * G + g0 + s;
+                            if (PERSIST && ++ps == ng) {
+                                ps = 0;
+                                pb += (int)gridDim.x;
+                            }
                             mbar_expect_tx(&full[i], kStageBytes);
                             bulk_g2s(st, qw + W4_HEADER_BYTES + rec * kRecWeights, kRecWeights,
                                      &full[i]);
@@ -399,37 +416,84 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             const float4 *xs4 = reinterpret_cast<const float4 *>(xsum) + tq;
             uint32_t phase = 0;                 // round of the ring, mod 2
             int s = 0;
-            for (; s + kStages <= ng; s += kStages) {
-#pragma unroll
-                for (int i = 0; i < kStages; ++i) {
-                    if (!mbar_wait(&full[i], phase)) goto consumer_failed;
+            if constexpr (PERSIST) {
+                // the per-token scale of x, undone on each row block's
+                // accumulators before its store (a power of two: exact)
+                float us0 = 1.f, us1 = 1.f;
+                if constexpr (FOLD) {
+                    if (2 * tq < M) us0 = token_scale(tok_max[2 * tq], true);
+                    if (2 * tq + 1 < M) us1 = token_scale(tok_max[2 * tq + 1], true);
+                }
+                int gi = 0;                     // group of the unit in its row block
+                int rb = b;                     // the unit's row block
+                auto unit = [&](int i) {
                     const GroupData g = read_group(smem + i * kStageBytes, warp, lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[i]);   // stage copied to registers
                     if constexpr (FOLD)
-                        group_mma_half_folded(acc, g, load_b(xrow + (s + i) * 64),
-                                              xs4[(s + i) * 4], zq, mask, mask_hi, magic);
+                        group_mma_half_folded(acc, g, load_b(xrow + gi * 64), xs4[gi * 4], zq,
+                                              mask, mask_hi, magic);
                     else
-                        group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, mask, magic);
-                }
-                phase ^= 1u;
-            }
+                        group_mma(acc, g, load_b(xrow + gi * 64), zq, mask, magic);
+                    if (++gi == ng) {           // row block rb done: store it
+                        gi = 0;
+                        acc[0] *= us0;
+                        acc[1] *= us1;
+                        acc[2] *= us0;
+                        acc[3] *= us1;
+                        store_out<F32OUT>(yv, acc, rb * kWarps + warp, lane, M, N, swiglu_I);
+                        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                        rb += (int)gridDim.x;
+                    }
+                };
+                for (; s + kStages <= U; s += kStages) {
 #pragma unroll
-            for (int i = 0; i < kStages - 1; ++i) {
-                if (s + i < ng) {
-                    if (!mbar_wait(&full[i], phase)) goto consumer_failed;
-                    const GroupData g = read_group(smem + i * kStageBytes, warp, lane);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[i]);
-                    if constexpr (FOLD)
-                        group_mma_half_folded(acc, g, load_b(xrow + (s + i) * 64),
-                                              xs4[(s + i) * 4], zq, mask, mask_hi, magic);
-                    else
-                        group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, mask, magic);
+                    for (int i = 0; i < kStages; ++i) {
+                        if (!mbar_wait(&full[i], phase)) goto consumer_failed;
+                        unit(i);
+                    }
+                    phase ^= 1u;
+                }
+#pragma unroll
+                for (int i = 0; i < kStages - 1; ++i) {
+                    if (s + i < U) {
+                        if (!mbar_wait(&full[i], phase)) goto consumer_failed;
+                        unit(i);
+                    }
+                }
+            } else {
+                for (; s + kStages <= ng; s += kStages) {
+#pragma unroll
+                    for (int i = 0; i < kStages; ++i) {
+                        if (!mbar_wait(&full[i], phase)) goto consumer_failed;
+                        const GroupData g = read_group(smem + i * kStageBytes, warp, lane);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[i]);   // stage copied to registers
+                        if constexpr (FOLD)
+                            group_mma_half_folded(acc, g, load_b(xrow + (s + i) * 64),
+                                                  xs4[(s + i) * 4], zq, mask, mask_hi, magic);
+                        else
+                            group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, mask, magic);
+                    }
+                    phase ^= 1u;
+                }
+#pragma unroll
+                for (int i = 0; i < kStages - 1; ++i) {
+                    if (s + i < ng) {
+                        if (!mbar_wait(&full[i], phase)) goto consumer_failed;
+                        const GroupData g = read_group(smem + i * kStageBytes, warp, lane);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[i]);
+                        if constexpr (FOLD)
+                            group_mma_half_folded(acc, g, load_b(xrow + (s + i) * 64),
+                                                  xs4[(s + i) * 4], zq, mask, mask_hi, magic);
+                        else
+                            group_mma(acc, g, load_b(xrow + (s + i) * 64), zq, mask, magic);
+                    }
                 }
             }
         }
-        if constexpr (FOLD) {
+        if constexpr (FOLD && !PERSIST) {
             // undo the per-token scale of x (a power of two: exact)
             const int m0 = 2 * tq, m1 = m0 + 1;
             const float u0 = m0 < M ? token_scale(tok_max[m0], true) : 1.f;
@@ -446,6 +510,7 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
         if (!ok && lane == 0) atomicOr(err, 1u);
     }
 
+    if constexpr (PERSIST) return;       // stored row block by row block
     wait_prerequisites();       // y may be read by the previous kernel in the stream
     const int t = b * kWarps + warp;
     if (S == 1) {
@@ -534,6 +599,24 @@ int active_clusters(const void *kern, cudaLaunchConfig_t cfg, int dev) {
     return n;
 }
 
+// Blocks of `kern` with `smem` bytes of dynamic shared memory resident per
+// SM, cached.
+int resident_blocks(const void *kern, size_t smem, int dev) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void *, size_t, int>, int> cache;
+    const auto key = std::make_tuple(kern, smem, dev);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    cache[key] = n;
+    return n;
+}
+
 }  // namespace
 
 cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zeros,
@@ -541,17 +624,9 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
                         const GemvShape &shape, int swiglu_I, int num_sms,
                         cudaStream_t stream) {
     const int S = shape.splits;
-    // Residency: three blocks per SM (more warps to hide the prologue and
-    // memory latency) where x's slice leaves room for them, with a ring of
-    // six stages or else five; otherwise two blocks with six.  The split S,
-    // and so the arithmetic, is the same whichever runs.
-    int variant = 0;                    // 0: two blocks, 6 stages; 1: three, 6; 2: three, 5
-    if (smem_plan(K, S, M, kStages).total <= kBlockSmemBudget3)
-        variant = 1;
-    else if (smem_plan(K, S, M, kStagesShort).total <= kBlockSmemBudget3)
-        variant = 2;
-    const SmemPlan plan = smem_plan(K, S, M, variant == 2 ? kStagesShort : kStages);
-    static bool attr_done[2][3][2][64] = {};
+    const long long blocks = (long long)row_blocks(N) * S;
+    const int sms = num_sms > 0 ? num_sms : 1;
+    const int need = blocks <= sms ? 1 : blocks <= 2LL * sms ? 2 : 3;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -560,23 +635,23 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     using Kern = void (*)(const char *, const char *, const char *, const __nv_bfloat16 *,
                           void *, uint32_t *, int, int, int, int, int, int, uint32_t,
                           uint32_t);
-    static const Kern kKernels[2][3][2] = {
-        {{gemv_kernel<false, 2, false, kStages>, gemv_kernel<false, 2, true, kStages>},
-         {gemv_kernel<false, 3, false, kStages>, gemv_kernel<false, 3, true, kStages>},
-         {gemv_kernel<false, 3, false, kStagesShort>, gemv_kernel<false, 3, true, kStagesShort>}},
-        {{gemv_kernel<true, 2, false, kStages>, gemv_kernel<true, 2, true, kStages>},
-         {gemv_kernel<true, 3, false, kStages>, gemv_kernel<true, 3, true, kStages>},
-         {gemv_kernel<true, 3, false, kStagesShort>, gemv_kernel<true, 3, true, kStagesShort>}}};
-    const Kern kern = kKernels[f32_out][variant][shape.fold];
-    if (!attr_done[f32_out][variant][shape.fold][dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ds.optin);
-        if (e != cudaSuccess) return e;
-        attr_done[f32_out][variant][shape.fold][dev] = true;
-    }
+    // [f32 out][variant][fold][persistent]; variant 0: two blocks per SM,
+    // 6 stages; 1: three, 6; 2: three, 5
+#define W4_GEMV_KERNELS(F, MB, ST)                                                      \
+    {{gemv_kernel<F, MB, false, ST, false>, gemv_kernel<F, MB, false, ST, true>},        \
+     {gemv_kernel<F, MB, true, ST, false>, gemv_kernel<F, MB, true, ST, true>}}
+    static const Kern kKernels[2][3][2][2] = {
+        {W4_GEMV_KERNELS(false, 2, kStages), W4_GEMV_KERNELS(false, 3, kStages),
+         W4_GEMV_KERNELS(false, 3, kStagesShort)},
+        {W4_GEMV_KERNELS(true, 2, kStages), W4_GEMV_KERNELS(true, 3, kStages),
+         W4_GEMV_KERNELS(true, 3, kStagesShort)}};
+#undef W4_GEMV_KERNELS
+    static const int kVariantStages[3] = {kStages, kStages, kStagesShort};
+    static bool attr_done[2][3][2][2][64] = {};
+
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)row_blocks(N), (unsigned)S, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = plan.total;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int na = 0;
@@ -589,35 +664,81 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
+
     // Residency.  A grid of one wave runs as long as its most loaded SM, so
     // it should spread evenly: at most ceil(blocks / SMs) blocks per SM.
     // Programmatic dependent launch starts blocks early in whatever slots
     // the previous kernel leaves free; with room for three blocks per SM
     // they stack up unevenly, so a grid that needs at most two per SM asks
-    // for enough shared memory that no more than that fit.  It then also
-    // overlaps its start with the previous kernel's end.  Grids that need
-    // three per SM launch without overlap (unless short); grids of several
-    // waves always overlap.
-    const long long blocks = (long long)row_blocks(N) * S;
-    const int sms = num_sms > 0 ? num_sms : 1;
-    const int need = blocks <= sms ? 1 : blocks <= 2LL * sms ? 2 : 3;
-    bool capped = false;
-    if (need < 3 && ds.per_sm > 0) {
+    // for enough shared memory that no more than that fit ("capped").  It
+    // then also overlaps its start with the previous kernel's end.  Grids
+    // that need three per SM launch without overlap (unless short); grids of
+    // several waves always overlap.  A block whose own shared memory
+    // already keeps a third one off the SM counts as capped as it stands.
+    // Ring depth: three blocks per SM (more warps to hide the prologue and
+    // memory latency) where x's slice leaves room for them, with a ring of
+    // six stages or else five; otherwise two blocks with six.  (A ring of
+    // twelve stages in half an SM measured slower at M = 1.)  The split S,
+    // and so the arithmetic, is the same whichever runs.
+    auto capped_smem = [&](const Kern kern, size_t total) -> size_t {
+        // shared memory that caps the grid at `need` blocks per SM, or 0
+        if (need >= 3 || ds.per_sm <= 0) return 0;
         const size_t pad = (size_t)(ds.per_sm / (need + 1) - ds.reserved + 16) / 16 * 16;
-        if (pad > plan.total && pad <= (size_t)ds.optin) {
-            cudaLaunchConfig_t padded = cfg;
-            padded.dynamicSmemBytes = pad;
-            // With clusters, only where the grid stays one wave with 10% of
-            // the cluster slots to spare: clusters are placed whole, within
-            // one GPC, and a grid that only just fits measured slower capped.
-            if (S == 1 ||
-                (long long)active_clusters((const void *)kern, padded, dev) * S * 10 >=
-                    blocks * 11) {
-                cfg.dynamicSmemBytes = pad;
-                capped = true;
-            }
+        const size_t want = pad > total ? pad : total;
+        if (want > (size_t)ds.optin || want + (size_t)ds.reserved > (size_t)(ds.per_sm / need))
+            return 0;
+        cudaLaunchConfig_t probe = cfg;
+        probe.dynamicSmemBytes = want;
+        // With clusters, only where the grid stays one wave with 10% of the
+        // cluster slots to spare: clusters are placed whole, within one GPC,
+        // and a grid that only just fits measured slower capped.
+        if (S > 1 &&
+            (long long)active_clusters((const void *)kern, probe, dev) * S * 10 < blocks * 11)
+            return 0;
+        return want;
+    };
+    auto prepare = [&](int v, int pers) -> cudaError_t {
+        const Kern kern = kKernels[f32_out][v][shape.fold][pers];
+        if (!attr_done[f32_out][v][shape.fold][pers][dev]) {
+            const cudaError_t r =
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ds.optin);
+            if (r != cudaSuccess) return r;
+            attr_done[f32_out][v][shape.fold][pers][dev] = true;
+        }
+        return cudaSuccess;
+    };
+    const int variant = smem_plan(K, S, M, kStages).total <= kBlockSmemBudget3        ? 1
+                        : smem_plan(K, S, M, kStagesShort).total <= kBlockSmemBudget3 ? 2
+                                                                                      : 0;
+    if ((e = prepare(variant, 0)) != cudaSuccess) return e;
+    size_t smem_bytes = smem_plan(K, S, M, kVariantStages[variant]).total;
+    bool capped = false;
+    {
+        const size_t c = capped_smem(kKernels[f32_out][variant][shape.fold][0], smem_bytes);
+        if (c > 0) {
+            smem_bytes = c;
+            capped = true;
         }
     }
+    // A grid of several waves without clusters runs persistent from three
+    // tokens on: one block per resident slot, each taking row blocks in
+    // turn, so that the x prologue (which grows with M) and the ring's
+    // start-up are paid once per slot rather than once per row block.  With
+    // fewer tokens the prologue is short and the hardware's dynamic
+    // assignment of row blocks to free slots measured faster.  The
+    // arithmetic of a row block is the same either way.
+    int pers = 0;
+    if (S == 1 && M >= kPersistMinTokens) {
+        if ((e = prepare(variant, 1)) != cudaSuccess) return e;
+        const int per_sm = resident_blocks((const void *)kKernels[f32_out][variant][shape.fold][1],
+                                           smem_bytes, dev);
+        if (per_sm > 0 && blocks > (long long)per_sm * sms) {
+            pers = 1;
+            cfg.gridDim.x = (unsigned)(per_sm * sms);
+        }
+    }
+    const Kern kern = kKernels[f32_out][variant][shape.fold][pers];
+    cfg.dynamicSmemBytes = smem_bytes;
     const bool overlap = capped || (size_t)K * (size_t)N / 2 < kOverlapBelowBytes ||
                          blocks > 3LL * sms;
     if (overlap) {

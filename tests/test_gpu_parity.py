@@ -140,6 +140,30 @@ def test_gemv_ragged_and_small(w4, M, K, N, path):
     tu.check_gemv(got32, got16, ref, mag, K, splits, f"edge {M},{K},{N} {path}", extra)
 
 
+@pytest.mark.parametrize("M,K,N", [(3, 1024, 64037), (8, 1024, 64037), (4, 768, 70001)])
+def test_gemv_persistent_grid(w4, M, K, N):
+    """Products of several waves without a K split run persistent from three
+    tokens on (each block takes row blocks in turn): oracle parity on sampled
+    rows including the ragged last row block, and every token's result equal
+    bit for bit to the single-token product, which runs one block per row
+    block."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    _, splits, fold = w4.gemv_config(K, N)
+    assert splits == 1 and (N + 127) // 128 > 3 * sms
+    assert fold == (K // 128 >= 8)
+    p = syn.make_problem(f"persist.{M}.{K}.{N}", K, N, M, seed=4)
+    got32, got16, packed = run_gemv(w4, p)
+    rows = sample_rows(N, np.random.default_rng(5))
+    ref, refabs = oracle_rows(p, rows)
+    mag, extra = bound_terms(w4, "cluster", p, rows, refabs)
+    tu.check_gemv(got32[:, rows], got16[:, rows], ref, mag, K, 1, f"persistent {M},{K},{N}",
+                  extra)
+    _, _, _, x = tu.to_device(p)
+    for r in range(M):
+        one = packed.gemv_f32(x[r:r + 1].contiguous()).cpu().numpy()
+        assert np.array_equal(one[0], got32[r]), r
+
+
 def test_split_paths_covered(w4):
     cfg = [w4.gemv_config(K, N) for (_, K, N, _, _) in syn.SHAPES]
     splits = {c[1] for c in cfg}
