@@ -60,6 +60,12 @@ constexpr size_t kBlockSmemBudget3 = 74 * 1024;     // three blocks per SM
 constexpr int kFoldMinGroups = 8;                   // see gemv_shape
 constexpr size_t kOverlapBelowBytes = 16u << 20;    // packed weights of a "short" product
 constexpr int kPersistMinTokens = 3;                // see launch_gemv
+constexpr int kWideMinTokens = 5;                   // see launch_gemv
+// Weight records a block requests before waiting for the previous kernel
+// (programmatic dependent launch); fewer than any ring holds, so that those
+// copies need no ring waits.
+constexpr int kPreIssue = 2;
+static_assert(kPreIssue < kStagesShort && kPreIssue < kStages, "pre-issued copies fit one round");
 
 struct SmemPlan {
     size_t x_off, x_row_bytes, red_off, xsum_off, tok_off, bar_off, total;
@@ -83,23 +89,17 @@ __host__ __device__ inline SmemPlan smem_plan(int K, int S, int M, int stages) {
     return p;
 }
 
-// Combine the K slices of a cluster in rank order 0, 1, ..., S-1 (all
-// threads of every block of the cluster call this once, after their loop).
-// Tile w is reduced by block w % S: every block first stores its partial of
-// tile w into that block's receive slot (rank, w / S) through distributed
-// shared memory, then one cluster barrier (release / acquire) makes all
-// partials visible, and each reducing warp adds its S slots from its own
-// shared memory.  No block reads another block's memory after the barrier,
-// so none has to wait for the others before exiting.
 // 2^e (or 2^-e for inverse) with e chosen so that 2^e times the bf16 value
-// whose magnitude bits are maxbits lies in [2^14, 2^15): the per-token scale
-// that brings x into fp16 range.  1 when the token's slice is all zero.
+// whose magnitude bits are maxbits lies in [2^14, 2^15) (e clamped to
+// [-126, 126]): the scale of a token's slice of x that brings it into fp16
+// range.  1 when the slice is all zero.
 __device__ __forceinline__ float token_scale(uint32_t maxbits, bool inverse) {
     if (maxbits == 0) return 1.f;
     int e = 141 - (int)(maxbits >> 7);                  // 14 - (bf16 exponent - 127)
     e = e > 126 ? 126 : (e < -126 ? -126 : e);
     return __uint_as_float((uint32_t)((inverse ? -e : e) + 127) << 23);
 }
+
 
 // Final store of a tile: y = W x, or the SwiGLU of the interleaved pairs.
 template <bool F32OUT>
@@ -111,6 +111,14 @@ __device__ __forceinline__ void store_out(void *yv, const float (&acc)[4], int t
         store_tile<F32OUT>(yv, acc, t, lane, M, N);
 }
 
+// Combine the K slices of a cluster in rank order 0, 1, ..., S-1 (all
+// threads of every block of the cluster call this once, after their loop).
+// Tile w is reduced by block w % S: every block first stores its partial of
+// tile w into that block's receive slot (rank, w / S) through distributed
+// shared memory, then one cluster barrier (release / acquire) makes all
+// partials visible, and each reducing warp adds its S slots from its own
+// shared memory.  No block reads another block's memory after the barrier,
+// so none has to wait for the others before exiting.
 template <bool F32OUT>
 __device__ __forceinline__ void cluster_combine(float a0, float a1, float a2, float a3, void *yv,
                                              unsigned char *red_bytes, int t, int S, int split,
@@ -140,8 +148,9 @@ __device__ __forceinline__ void cluster_combine(float a0, float a1, float a2, fl
 
 // PERSIST (split S = 1 only): block c takes row blocks c, c + gridDim.x, ...
 // in turn through one ring and one x prologue; otherwise block (b, split)
-// takes row block b's K slice `split`.
-template <bool F32OUT, int MIN_BLOCKS, bool FOLD, int STAGES, bool PERSIST>
+// takes row block b's K slice `split`.  WIDE (FOLD only): the x prologue's
+// work is spread over (group, token) pairs (see launch_gemv for its use).
+template <bool F32OUT, int MIN_BLOCKS, bool FOLD, int STAGES, bool PERSIST, bool WIDE>
 __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
 gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             const char *__restrict__ zp, const __nv_bfloat16 *__restrict__ x,
@@ -173,6 +182,9 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
         }
         mbar_init(xbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (FOLD && WIDE)   // per-token maxima of |x| (the prologue's atomicMax)
+            for (int m = 0; m < W4_MAX_TOKENS; ++m)
+                reinterpret_cast<uint32_t *>(smem + plan.tok_off)[m] = 0u;
         reinterpret_cast<uint32_t *>(xbar + 1)[0] = nib_mask;
         reinterpret_cast<uint32_t *>(xbar + 1)[1] = bf16_magic;
     }
@@ -253,9 +265,13 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
     } else {
         // ---- consumers: warp w owns tile 8b + w ----
         const int gq = lane >> 2, tq = lane & 3;
+        // Fold only: per group and token X01, X23 (float [gmax][4 token
+        // pairs][4]), and per token the largest |x| of the slice (bf16 bits).
+        // Sums of tokens >= M are never written: the accumulators they feed
+        // belong to token columns that are not stored.
         float *xsum = reinterpret_cast<float *>(smem + plan.xsum_off);
         uint32_t *tok_max = reinterpret_cast<uint32_t *>(smem + plan.tok_off);
-        if (FOLD) {
+        if (FOLD && !WIDE) {
             // sums of tokens >= M stay zero; maxima start at zero
             for (int i = threadIdx.x; i < ng * 16; i += kWarps * 32) xsum[i] = 0.f;
             if (threadIdx.x < W4_MAX_TOKENS) tok_max[threadIdx.x] = 0u;
@@ -286,7 +302,139 @@ gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
             // Every consumer thread takes part in the barriers below even if
             // its wait gave up.
             const bool x_ok = mbar_wait(xbar, 0);
-            if constexpr (FOLD) {
+            if constexpr (FOLD && WIDE) {
+                // The folded product runs on fp16 operands: x is scaled per
+                // token by a power of two 2^e (exact) that brings the largest
+                // |x| of the token's slice into [2^14, 2^15), then rounded to
+                // fp16 in place; per group and token the two sums X01
+                // (k mod 16 < 8) and X23 (k mod 16 >= 8) of the scaled values
+                // feed the zero-point term of group_mma_half_folded (the fp16
+                // values equal them except below the fp16 normal range, 2^28
+                // under the token's largest).  The fp32 arithmetic is fixed:
+                // per 16-aligned block of the group and half (first or last
+                // eight values), the values at even and at odd positions are
+                // summed left to right in two packed lanes and the two lane
+                // sums added; then over the eight blocks the pairwise tree
+                // ((p0+p1)+(p2+p3))+((p4+p5)+(p6+p7)).  Only the assignment
+                // of that work to threads depends on the number of (group,
+                // token) pairs: tpp threads per pair, each with per = 8 / tpp
+                // consecutive blocks, joined by shuffles that follow the same
+                // tree.  (The wide prologue; the narrow one below takes the
+                // maxima token by token.  Both compute the same numbers.)
+                const int pairs = ng * M;
+                int tpp = 8;
+                while (tpp > 1 && pairs * tpp > kWarps * 32) tpp >>= 1;
+                const int per = 8 / tpp;
+                // (1) the largest magnitude of each token's slice, as bf16 bits
+                // (whose integer order is the order of the magnitudes)
+                if (x_ok) {
+                    for (int base = 0; base < pairs * tpp; base += kWarps * 32) {
+                        const int idx = base + (int)threadIdx.x;
+                        const int pair = idx / tpp, sub = idx - pair * tpp;
+                        const bool live = pair < pairs;
+                        const int gl = live ? pair / M : 0, m = live ? pair - gl * M : 0;
+                        const uint4 *blk = reinterpret_cast<const uint4 *>(
+                            xs + (size_t)m * plan.x_row_bytes + (size_t)gl * kGroup * 2 +
+                            (size_t)sub * per * 32);
+                        uint32_t mx2 = 0u;              // two 16-bit maxima
+                        if (live) {
+#pragma unroll
+                            for (int j = 0; j < 2 * per; ++j) {
+                                const uint4 v = blk[j];
+                                mx2 = __vmaxu2(mx2, v.x & 0x7FFF7FFFu);
+                                mx2 = __vmaxu2(mx2, v.y & 0x7FFF7FFFu);
+                                mx2 = __vmaxu2(mx2, v.z & 0x7FFF7FFFu);
+                                mx2 = __vmaxu2(mx2, v.w & 0x7FFF7FFFu);
+                            }
+                        }
+                        uint32_t mx = max(mx2 & 0xFFFFu, mx2 >> 16);
+                        for (int o = 1; o < tpp; o <<= 1)
+                            mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+                        if (sub == 0 && live && mx) atomicMax(&tok_max[m], mx);
+                    }
+                }
+                consumer_sync();
+                // (2) scale, convert in place, sum
+                if (x_ok) {
+                    for (int base = 0; base < pairs * tpp; base += kWarps * 32) {
+                        const int idx = base + (int)threadIdx.x;
+                        const int pair = idx / tpp, sub = idx - pair * tpp;
+                        const bool live = pair < pairs;
+                        const int gl = live ? pair / M : 0, m = live ? pair - gl * M : 0;
+                        uint4 *blk = reinterpret_cast<uint4 *>(
+                            xs + (size_t)m * plan.x_row_bytes + (size_t)gl * kGroup * 2 +
+                            (size_t)sub * per * 32);
+                        float v01 = 0.f, v23 = 0.f;
+                        if (live) {
+                            const float sc = token_scale(tok_max[m], false);
+                            const unsigned long long sc2 =
+                                ((unsigned long long)__float_as_uint(sc) << 32) | __float_as_uint(sc);
+                            float l01[3], l23[3];   // pending subtree sums, levels 0..2
+#pragma unroll
+                            for (int j = 0; j < per; ++j) {
+                                const uint4 u0 = blk[2 * j], u1 = blk[2 * j + 1];
+                                const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w,
+                                                       u1.x, u1.y, u1.z, u1.w};
+                                uint32_t h[8];
+                                unsigned long long a01 = 0ull, a23 = 0ull;
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    // the pair as fp32 (bf16 is the top half of fp32), scaled
+                                    const unsigned long long f = f32x2_mul(
+                                        ((unsigned long long)(w[e] & 0xFFFF0000u) << 32) |
+                                            (unsigned long long)(w[e] << 16),
+                                        sc2);
+                                    const __half2 hv = __floats2half2_rn(f32x2_lo(f), f32x2_hi(f));
+                                    h[e] = *reinterpret_cast<const uint32_t *>(&hv);
+                                    if (e < 4)
+                                        a01 = e == 0 ? f : f32x2_add(a01, f);
+                                    else
+                                        a23 = e == 4 ? f : f32x2_add(a23, f);
+                                }
+                                blk[2 * j] = make_uint4(h[0], h[1], h[2], h[3]);
+                                blk[2 * j + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+                                // leaf j of the pairwise tree over this thread's
+                                // blocks; after the last leaf v is the subtree
+                                v01 = f32x2_lo(a01) + f32x2_hi(a01);
+                                v23 = f32x2_lo(a23) + f32x2_hi(a23);
+                                if (j & 1) {
+                                    v01 = l01[0] + v01;
+                                    v23 = l23[0] + v23;
+                                    if (j & 2) {
+                                        v01 = l01[1] + v01;
+                                        v23 = l23[1] + v23;
+                                        if (j & 4) {
+                                            v01 = l01[2] + v01;
+                                            v23 = l23[2] + v23;
+                                        } else {
+                                            l01[2] = v01;
+                                            l23[2] = v23;
+                                        }
+                                    } else {
+                                        l01[1] = v01;
+                                        l23[1] = v23;
+                                    }
+                                } else {
+                                    l01[0] = v01;
+                                    l23[0] = v23;
+                                }
+                            }
+                        }
+                        // the pair's tpp subtrees
+                        for (int o = 1; o < tpp; o <<= 1) {
+                            v01 += __shfl_xor_sync(0xFFFFFFFFu, v01, o);
+                            v23 += __shfl_xor_sync(0xFFFFFFFFu, v23, o);
+                        }
+                        if (sub == 0 && live) {
+                            float *xg = xsum + gl * 16 + (m >> 1) * 4 + (m & 1);
+                            xg[0] = v01;
+                            xg[2] = v23;
+                        }
+                    }
+                }
+                consumer_sync();
+            }
+            if constexpr (FOLD && !WIDE) {
                 // The folded product runs on fp16 operands: x is scaled per
                 // token by a power of two (exact) into fp16 range.  (1) The
                 // largest |x| of each token's slice, as bf16 magnitude bits
@@ -635,19 +783,22 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     using Kern = void (*)(const char *, const char *, const char *, const __nv_bfloat16 *,
                           void *, uint32_t *, int, int, int, int, int, int, uint32_t,
                           uint32_t);
-    // [f32 out][variant][fold][persistent]; variant 0: two blocks per SM,
-    // 6 stages; 1: three, 6; 2: three, 5
-#define W4_GEMV_KERNELS(F, MB, ST)                                                      \
-    {{gemv_kernel<F, MB, false, ST, false>, gemv_kernel<F, MB, false, ST, true>},        \
-     {gemv_kernel<F, MB, true, ST, false>, gemv_kernel<F, MB, true, ST, true>}}
-    static const Kern kKernels[2][3][2][2] = {
+    // [f32 out][variant][arithmetic][persistent]; variant 0: two blocks per
+    // SM, 6 stages; 1: three, 6; 2: three, 5; arithmetic 0: exact q - z,
+    // 1: folded, 2: folded with the wide x prologue
+#define W4_GEMV_KERNELS(F, MB, ST)                                                        \
+    {{gemv_kernel<F, MB, false, ST, false, false>, gemv_kernel<F, MB, false, ST, true, false>}, \
+     {gemv_kernel<F, MB, true, ST, false, false>, gemv_kernel<F, MB, true, ST, true, false>},   \
+     {gemv_kernel<F, MB, true, ST, false, true>, gemv_kernel<F, MB, true, ST, true, true>}}
+    static const Kern kKernels[2][3][3][2] = {
         {W4_GEMV_KERNELS(false, 2, kStages), W4_GEMV_KERNELS(false, 3, kStages),
          W4_GEMV_KERNELS(false, 3, kStagesShort)},
         {W4_GEMV_KERNELS(true, 2, kStages), W4_GEMV_KERNELS(true, 3, kStages),
          W4_GEMV_KERNELS(true, 3, kStagesShort)}};
 #undef W4_GEMV_KERNELS
     static const int kVariantStages[3] = {kStages, kStages, kStagesShort};
-    static bool attr_done[2][3][2][2][64] = {};
+    static bool attr_done[2][3][3][2][64] = {};
+    int arith = shape.fold ? 1 : 0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)row_blocks(N), (unsigned)S, 1);
@@ -698,12 +849,12 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
         return want;
     };
     auto prepare = [&](int v, int pers) -> cudaError_t {
-        const Kern kern = kKernels[f32_out][v][shape.fold][pers];
-        if (!attr_done[f32_out][v][shape.fold][pers][dev]) {
+        const Kern kern = kKernels[f32_out][v][arith][pers];
+        if (!attr_done[f32_out][v][arith][pers][dev]) {
             const cudaError_t r =
                 cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ds.optin);
             if (r != cudaSuccess) return r;
-            attr_done[f32_out][v][shape.fold][pers][dev] = true;
+            attr_done[f32_out][v][arith][pers][dev] = true;
         }
         return cudaSuccess;
     };
@@ -714,7 +865,7 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     size_t smem_bytes = smem_plan(K, S, M, kVariantStages[variant]).total;
     bool capped = false;
     {
-        const size_t c = capped_smem(kKernels[f32_out][variant][shape.fold][0], smem_bytes);
+        const size_t c = capped_smem(kKernels[f32_out][variant][arith][0], smem_bytes);
         if (c > 0) {
             smem_bytes = c;
             capped = true;
@@ -730,14 +881,22 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     int pers = 0;
     if (S == 1 && M >= kPersistMinTokens) {
         if ((e = prepare(variant, 1)) != cudaSuccess) return e;
-        const int per_sm = resident_blocks((const void *)kKernels[f32_out][variant][shape.fold][1],
+        const int per_sm = resident_blocks((const void *)kKernels[f32_out][variant][arith][1],
                                            smem_bytes, dev);
         if (per_sm > 0 && blocks > (long long)per_sm * sms) {
             pers = 1;
             cfg.gridDim.x = (unsigned)(per_sm * sms);
         }
     }
-    const Kern kern = kKernels[f32_out][variant][shape.fold][pers];
+    // The folded product's x prologue: from five tokens on, one-wave grids
+    // spread it over (group, token) pairs (faster there by 2-11 % at M = 5-8);
+    // with fewer tokens, and in persistent grids (which run it once per
+    // slot), the token-by-token prologue measured faster.
+    if (arith == 1 && !pers && M >= kWideMinTokens) {
+        arith = 2;
+        if ((e = prepare(variant, 0)) != cudaSuccess) return e;
+    }
+    const Kern kern = kKernels[f32_out][variant][arith][pers];
     cfg.dynamicSmemBytes = smem_bytes;
     const bool overlap = capped || (size_t)K * (size_t)N / 2 < kOverlapBelowBytes ||
                          blocks > 3LL * sms;
@@ -752,7 +911,7 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     return cudaLaunchKernelEx(&cfg, kern, q, static_cast<const char *>(scales),
                               static_cast<const char *>(zeros),
                               reinterpret_cast<const __nv_bfloat16 *>(x), y, err, M, K, N, S,
-                              overlap ? 2 : 0, swiglu_I, 0x000F000Fu,
+                              overlap ? kPreIssue : 0, swiglu_I, 0x000F000Fu,
                               shape.fold ? 0x64006400u : 0x43004300u);
 }
 

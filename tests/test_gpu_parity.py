@@ -164,6 +164,40 @@ def test_gemv_persistent_grid(w4, M, K, N):
         assert np.array_equal(one[0], got32[r]), r
 
 
+def _scale_bf16(bits, k):
+    """bf16 bit patterns times 2^k (exponent field moved by k; zeros stay)."""
+    b = bits.astype(np.int32)
+    e = (b >> 7) & 0xFF
+    assert ((e == 0) | ((e + k > 0) & (e + k < 255))).all()
+    return np.where(e == 0, b, b + (k << 7)).astype(bits.dtype)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M", [3, 6])
+def test_gemv_x_dynamic_range(w4, path, M):
+    """x far outside the fp16 range, tiny, zero and mixed within one group:
+    the folded fp16 path scales each token by a power of two, so the result
+    stays within the bound (which counts the fp16 rounding of values more
+    than 2^28 below their token's largest).  M = 3 and 6 take the two x
+    prologues of the folded path."""
+    K, N = 8192, 384
+    p = syn.make_problem("xrange", K, N, M, seed=12)
+    x = p.x.copy()
+    x[0, 0:128] = _scale_bf16(x[0, 0:128], 40)          # |x| up to ~2^42
+    x[0, 128:256] = _scale_bf16(x[0, 128:256], -60)     # |x| ~ 2^-60
+    x[0, 256:384] = 0                                   # an all-zero group
+    x[1, 384:448] = _scale_bf16(x[1, 384:448], 30)      # 2^30 next to 2^-30 in one group
+    x[1, 448:512] = _scale_bf16(x[1, 448:512], -30)
+    x[2, :] = _scale_bf16(x[2, :], -100)                # a whole token tiny
+    p = syn.Problem(p.name, M, K, N, p.qweight, p.scales, p.zeros, x)
+    got32, got16, _ = run_gemv(w4, p, path=path)
+    assert np.isfinite(got32).all()
+    ref, refabs = oracle.gemv_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N, with_abs=True)
+    mag, extra = bound_terms(w4, path, p, None, refabs)
+    tu.check_gemv(got32, got16, ref, mag, K, path_splits(w4, path, K, N), f"x range {path}",
+                  extra)
+
+
 def test_split_paths_covered(w4):
     cfg = [w4.gemv_config(K, N) for (_, K, N, _, _) in syn.SHAPES]
     splits = {c[1] for c in cfg}
