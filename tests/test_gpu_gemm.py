@@ -41,6 +41,21 @@ def test_gemm_parity(w4, M, K, N):
                   tu.FOLD_EXTRA_STEPS if fold else 0)
 
 
+def test_gemm_multi_wave_rows_equal_single_token_gemv(w4):
+    """A product of several waves without a K split: passes of 8 and of 4
+    tokens run the persistent grid, the single-token products one block per
+    row block; every row is the same bit for bit."""
+    M, K, N = 20, 1024, 64037
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert w4.gemv_config(K, N)[1] == 1 and (N + 127) // 128 > 3 * sms
+    p, packed, x = setup(w4, "gemm.multiwave", K, N, M, 3)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x, y, M, K, N)
+    for r in (0, 9, 16, 19):
+        one = packed.gemv_f32(x[r:r + 1].contiguous())
+        assert torch.equal(one[0], y[r]), r
+
+
 def test_gemm_rows_equal_single_token_gemv(w4):
     M, K, N = 40, 3584, 37888
     p, packed, x = setup(w4, "gemm.rows", K, N, M, 2)

@@ -175,20 +175,26 @@ def _scale_bf16(bits, k):
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("M", [3, 6])
 def test_gemv_x_dynamic_range(w4, path, M):
-    """x far outside the fp16 range, tiny, zero and mixed within one group:
-    the folded fp16 path scales each token by a power of two, so the result
-    stays within the bound (which counts the fp16 rounding of values more
-    than 2^28 below their token's largest).  M = 3 and 6 take the two x
-    prologues of the folded path."""
+    """x far outside the fp16 range, tiny, zero and mixed within one group,
+    and ordinary tokens with values below 2^-17: the folded fp16 path scales
+    each token by a power of two into fp16 range, so the result stays within
+    the bound (which counts the fp16 rounding of values more than 2^28 below
+    their token's largest).  M = 3 and 6 take the two x prologues of the
+    folded path."""
     K, N = 8192, 384
     p = syn.make_problem("xrange", K, N, M, seed=12)
     x = p.x.copy()
     x[0, 0:128] = _scale_bf16(x[0, 0:128], 40)          # |x| up to ~2^42
-    x[0, 128:256] = _scale_bf16(x[0, 128:256], -60)     # |x| ~ 2^-60
+    x[0, 128:256] = _scale_bf16(x[0, 128:256], -60)     # a group ~2^-60 beside it
     x[0, 256:384] = 0                                   # an all-zero group
     x[1, 384:448] = _scale_bf16(x[1, 384:448], 30)      # 2^30 next to 2^-30 in one group
     x[1, 448:512] = _scale_bf16(x[1, 448:512], -30)
-    x[2, :] = _scale_bf16(x[2, :], -100)                # a whole token tiny
+    x[2, ::37] = 0x3400                                 # 2^-23 in an ordinary token
+    x[2, 5::41] = 0
+    if M > 3:
+        x[3, :] = _scale_bf16(x[3, :], -100)            # a whole token tiny
+        x[4, :] = _scale_bf16(x[4, :], -3)              # largest ~0.4
+        x[5, :] = _scale_bf16(x[5, :], -6)              # largest ~0.05
     p = syn.Problem(p.name, M, K, N, p.qweight, p.scales, p.zeros, x)
     got32, got16, _ = run_gemv(w4, p, path=path)
     assert np.isfinite(got32).all()
@@ -322,6 +328,9 @@ def test_graph_capture_replay(w4, path):
     assert torch.equal(y, y_eager)
 
 
+# The capture below records nothing on purpose (the repack refuses to run
+# under capture), so torch's "graph is empty" warning is expected.
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
 def test_repack_rejects_bad_zero_and_capture(w4):
     K, N = 256, 32
     p = syn.make_problem("badz", K, N, 1, seed=11)

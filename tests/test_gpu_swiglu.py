@@ -82,6 +82,22 @@ def test_swiglu_parity(w4, M, K, I):
     check(got32[:, cols], got16[:, cols], y, b, f"M={M} K={K} I={I}")
 
 
+def test_swiglu_persistent_grid(w4):
+    """Enough rows for several waves without a K split, from three tokens on:
+    the persistent grid stores the activation row block by row block."""
+    M, K, I = 4, 1024, 30001
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    _, S, fold = w4.gemv_config(K, 16 * ((I + 7) // 8))
+    rows = 16 * ((I + 7) // 8)                 # kernel rows of the interleaved layout
+    assert S == 1 and fold and (rows + 127) // 128 > 3 * sms
+    p = syn.make_problem(f"swiglu.persist.{K}.{I}", K, 2 * I, M, seed=7)
+    got32, got16, _ = run(w4, p, I)
+    cols = np.unique(np.concatenate([np.arange(64), np.arange(I - 64, I),
+                                     np.random.default_rng(8).choice(I, 1024, replace=False)]))
+    y, b = bound(w4, p, I, cols)
+    check(got32[:, cols], got16[:, cols], y, b, f"persistent M={M} K={K} I={I}")
+
+
 def test_swiglu_matches_plain_gemv_then_activation(w4):
     """The interleaved layout only reorders rows: the gate and up products
     are the plain w4_gemv_f32 results (same split, same arithmetic)."""
