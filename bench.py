@@ -192,6 +192,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of the ranks' values, returned on every rank (x itself when
+    there is one rank).  The timing of a multi-GPU run is its slowest rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbps(world: int, bytes_per_rank_step: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank streams its own replica's bytes per
+    step (weak scaling), and the step takes the slowest rank's time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def reference_arm(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -313,10 +331,7 @@ def gpu_arm(args):
     ms = ev0.elapsed_time(ev1) / args.steps
     gu_launch_us = 1e3 * g0.elapsed_time(g1) / (reps * len(gu))
 
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # end to end through the public API: pinned host x in, device chain, host y out
     h_x = {k: v.cpu().pin_memory() for k, v in xs.items()}
@@ -341,14 +356,11 @@ def gpu_arm(args):
     e1.synchronize()
     t_host = (time.perf_counter() - t_host0) / e2e_steps
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     bytes_step = chain_bytes()
     peak, peak_kind = read_peaks()
-    value = world * bytes_step / (ms * 1e-3) / 1e9
+    value = job_gbps(world, bytes_step, ms)
     gu_bytes = canonical_bytes(1, 3584, 37888)
     achieved = gu_bytes / (gu_launch_us * 1e-6) / 1e9
     result = None
@@ -373,7 +385,7 @@ def gpu_arm(args):
                          "kernel": "w4 gemv, gate_up 3584->37888, M=1",
                          "bytes_per_launch": gu_bytes,
                          "launch_us": round(gu_launch_us, 3), "peak_kind": peak_kind},
-            "e2e": {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "e2e": {"value": round(job_gbps(world, bytes_step, e2e_ms), 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms, 5), "host_ms_per_step": round(1e3 * t_host, 5)},
             "gpu_launches": args.steps * launches_per_step,
