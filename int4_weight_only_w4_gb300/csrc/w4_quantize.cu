@@ -24,8 +24,13 @@
 // the product each rounded to nearest, is within |w/s| * 2^-22.4 of the
 // correctly rounded quotient the rule asks for, so the two round to different
 // integers only if t lies within that distance of a half-integer.  Where t is
-// within |t| * 2^-21 of one, the quotient is taken with the correctly
-// rounded division instead; elsewhere rint(t) is the rule's value.
+// within T * 2^-21 of one (T = the group's largest |w| times rcp(s), rounded
+// the same way, so T >= |t|), the quotient is taken with the correctly
+// rounded division instead; elsewhere rint(t) is the rule's value.  rint(t)
+// comes from one addition: t + 1.5 * 2^23 rounds to nearest (ties to even)
+// at unit spacing for |t| < 2^22 (here |t| <= 32), so its low bits are
+// rint(t) as an integer and subtracting 1.5 * 2^23 again gives it exactly as
+// a float.
 #include <cuda_fp16.h>
 
 #include "w4_internal.cuh"
@@ -40,13 +45,15 @@ __device__ __forceinline__ float clampf(float v, float a, float b) {
     return fminf(fmaxf(v, a), b);
 }
 
-// rint(x / s), with r = rcp_rn(s) (see above).
-__device__ __forceinline__ float rint_div(float x, float s, float r) {
+// rint(x / s) as an integer, with r = rcp_rn(s) and tol = T * 2^-21 (see above).
+__device__ __forceinline__ int rint_div(float x, float s, float r, float tol) {
+    constexpr float kMagic = 12582912.f;                // 1.5 * 2^23
     const float t = __fmul_rn(x, r);
-    const float n = rintf(t);
+    const float y = __fadd_rn(t, kMagic);
+    const float n = __fsub_rn(y, kMagic);
     // distance from t to the nearest half-integer is 0.5 - |t - n|
-    if (0.5f - fabsf(t - n) <= fabsf(t) * 0x1p-21f) return rintf(__fdiv_rn(x, s));
-    return n;
+    if (0.5f - fabsf(t - n) <= tol) return (int)rintf(__fdiv_rn(x, s));
+    return (int)(__float_as_uint(y) - __float_as_uint(kMagic));
 }
 
 template <bool SYMMETRIC>
@@ -102,21 +109,25 @@ quantize_kernel(const uint4 *__restrict__ w, long long groups,
             const __half sh = __float2half_rn(s32);
             const float s = __half2float(sh);
             const float r = s == 0.f ? 0.f : __frcp_rn(s);
+            // T * 2^-21 with T = rcp(s) times the largest |w| (rounded as t is)
+            const float tol =
+                __fmul_rn(symmetric ? amax : fmaxf(-lo, hi), r) * 0x1p-21f;
             float z;
             if (s == 0.f)
                 z = symmetric ? 8.f : 0.f;
             else
                 z = symmetric ? 8.f : clampf(rintf(__fdiv_rn(-lo, s)), 0.f, 15.f);
+            const int zi = (int)z;
             uint32_t word = 0u;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                float q;
+                int q;
                 if (s == 0.f) {
-                    q = z;
+                    q = zi;
                 } else {
-                    const float c = rint_div(x[j], s, r);
-                    q = symmetric ? clampf(c, -8.f, 7.f) + 8.f
-                                  : clampf(clampf(c, -16.f, 16.f) + z, 0.f, 15.f);
+                    const int c = rint_div(x[j], s, r, tol);
+                    q = symmetric ? min(max(c, -8), 7) + 8
+                                  : min(max(min(max(c, -16), 16) + zi, 0), 15);
                 }
                 word |= (uint32_t)q << (4 * j);
             }
