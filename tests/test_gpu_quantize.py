@@ -106,3 +106,26 @@ def test_quantize_argument_errors(w4):
     with pytest.raises(w4.W4Error) as e:
         w4.quantize(buf[1:1 + N * K], K, N, 0, qw, sc, zp)
     assert e.value.status == w4.Status.INVALID_ARG
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_quantize_outputs_at_minimum_alignment(w4, mode):
+    """qweight need only be 4-byte aligned, scales 2-byte aligned and zeros
+    not aligned at all: outputs written one element past aligned buffers
+    equal the aligned call's."""
+    N, K = 65, 1152
+    w = weights(N, K, seed=77 + mode)
+    want = gpu_quantize(w4, w, mode)
+    wd = torch.from_numpy(np.ascontiguousarray(w).view(np.int16)).cuda()
+    qw = torch.empty(N * K // 8 + 1, dtype=torch.int32, device="cuda")
+    sc = torch.empty(N * K // 128 + 1, dtype=torch.int16, device="cuda")
+    zp = torch.empty(N * K // 128 + 1, dtype=torch.uint8, device="cuda")
+    assert qw[1:].data_ptr() % 8 == 4
+    w4.quantize(wd, K, N, mode, qw[1:], sc[1:], zp[1:])
+    torch.cuda.synchronize()
+    got = (qw[1:].cpu().numpy().view(np.uint32).reshape(N, K // 8),
+           sc[1:].cpu().numpy().view(np.uint16).reshape(N, K // 128),
+           zp[1:].cpu().numpy().reshape(N, K // 128))
+    for g, o, name in zip(got, want, ("qweight", "scales", "zeros")):
+        assert np.array_equal(g, o), name
+
