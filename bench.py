@@ -704,6 +704,64 @@ def quantize_arm(args):
     return 0
 
 
+def small_chain_arm(args):
+    """A second, smaller chain: the 24 layers of the 0.5B-shape model (188 MB
+    of weights, about 1.5x L2, so much of it can stay in L2 between steps;
+    the small GEMVs are latency-bound).  Reported as its own line, not as the
+    headline."""
+    import torch
+
+    from int4_weight_only_w4_gb300 import w4
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    xs, packed, ys = {}, [], []
+    for kind, K, N in syn.LAYER_05B:
+        xs[kind] = torch.from_numpy(syn.make_x(f"chain05b.x.{kind}", 1, K, SEED)
+                                    .view(np.int16)).to(dev).view(torch.bfloat16)
+    for layer in range(syn.LAYERS_05B):
+        for kind, K, N in syn.LAYER_05B:
+            qw, sc, zp = syn.make_weights(f"chain05b.L{layer}.{kind}", K, N, SEED, SCALES)
+            packed.append((kind, w4.pack(torch.from_numpy(qw.view(np.int32)).to(dev),
+                                         torch.from_numpy(sc.view(np.int16)).to(dev),
+                                         torch.from_numpy(zp).to(dev), K, N)))
+            ys.append(torch.empty((1, N), dtype=torch.bfloat16, device=dev))
+    stream = torch.cuda.Stream(device=dev)
+
+    def chain_calls():
+        for (kind, pw), y in zip(packed, ys):
+            pw.gemv(xs[kind], y, stream=stream)
+
+    with torch.cuda.stream(stream):
+        chain_calls()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        chain_calls()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    bytes_step = syn.LAYERS_05B * sum(canonical_bytes(1, K, N) for _, K, N in syn.LAYER_05B)
+    peak, peak_kind = read_peaks()
+    value = bytes_step / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "workload": "qwen0.5b-shape 24-layer W4 GEMV chain, M=1, CUDA-graph replay "
+                    "(second data point; weights about 1.5x L2)",
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
+        "tok_per_s": round(1e3 / ms, 1), "bytes_per_step": bytes_step,
+        "gemvs_per_step": len(packed), "steps": args.steps, "warmup": args.warmup,
+        "frac_of_peak": round(value / peak, 4), "peak_kind": peak_kind}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -718,6 +776,8 @@ def main():
                     help="per-call timing of the fused gate/up + SwiGLU product")
     ap.add_argument("--quantize", action="store_true",
                     help="per-call timing of w4_quantize on the workloads' weight shapes")
+    ap.add_argument("--chain-05b", action="store_true",
+                    help="time the 24-layer 0.5B-shape chain (a second, smaller data point)")
     ap.add_argument("--per-shape", action="store_true",
                     help="per-call timing of every workload shape instead of the chain")
     ap.add_argument("--kernel-case", default=None,
@@ -733,6 +793,8 @@ def main():
         return swiglu_arm(args)
     if args.gemm:
         return gemm_arm(args)
+    if args.chain_05b:
+        return small_chain_arm(args)
     if args.per_shape or args.kernel_case:
         return per_shape_arm(args)
     return gpu_arm(args)

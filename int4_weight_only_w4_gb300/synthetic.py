@@ -183,6 +183,12 @@ LAYER_7B = [("qkv", 3584, 4608), ("o", 3584, 3584), ("gate_up", 3584, 37888),
             ("down", 18944, 3584)]
 LAYERS_7B = 28
 
+# One decoder layer of the 0.5B-shape model (hidden 896, intermediate 4864,
+# 14 query and 2 key/value heads of 64), which has 24 layers.
+LAYER_05B = [("qkv", 896, 1152), ("o", 896, 896), ("gate_up", 896, 9728),
+             ("down", 4864, 896)]
+LAYERS_05B = 24
+
 
 def shape(name: str):
     for s in SHAPES:
