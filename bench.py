@@ -21,6 +21,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import random
 import statistics
 import subprocess
 import sys
@@ -415,8 +416,11 @@ def gpu_arm(args):
 
 def per_shape_arm(args):
     """Per-call timing of every workload shape: R calls over rotating weight
-    copies (so that the weights never sit in L2) captured in one CUDA graph.
-    Prints one JSON line per (shape, M)."""
+    copies (so that the weights never sit in L2) captured in one CUDA graph,
+    the graph replayed 25 times after the warm-up; per-call time = replay
+    time / R, reported as the median (and mean, p90, p99, and a flag when
+    the mean is more than 15 % above the median).  The shapes run in a
+    shuffled (seeded) order.  Prints one JSON line per (shape, M)."""
     import torch
 
     from int4_weight_only_w4_gb300 import w4
@@ -425,6 +429,7 @@ def per_shape_arm(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     peak, peak_kind = read_peaks()
     names = [args.kernel_case] if args.kernel_case else [s[0] for s in syn.SHAPES]
+    random.Random(SEED).shuffle(names)
     stream = torch.cuda.Stream(device=dev)
     for name in names:
         _, K, N, Ms, srange = syn.shape(name)
@@ -463,7 +468,7 @@ def per_shape_arm(args):
             with torch.cuda.stream(stream):
                 for _ in range(args.warmup):
                     g.replay()
-                for _ in range(5):
+                for _ in range(25):
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
@@ -472,6 +477,8 @@ def per_shape_arm(args):
                     e1.synchronize()
                     times.append(e0.elapsed_time(e1) * 1e3 / reps)
             us = statistics.median(times)
+            mean = statistics.fmean(times)
+            pct = np.percentile(times, [90, 99])
             # eager single call (includes launch overhead through the binding)
             t0 = time.perf_counter()
             for _ in range(20):
@@ -485,7 +492,10 @@ def per_shape_arm(args):
                               "peak_kind": peak_kind, "bytes": b, "copies": copies,
                               "calls_per_graph": reps, "splits": w4.gemv_config(K, N)[1],
                               "eager_us_per_call": round(eager_us, 2),
-                              "runs_us": [round(t, 3) for t in times]}), flush=True)
+                              "mean_us": round(mean, 3), "p90_us": round(float(pct[0]), 3),
+                              "p99_us": round(float(pct[1]), 3),
+                              "mean_above_median_15pct": mean > 1.15 * us,
+                              "replays": len(times)}), flush=True)
         del packs, base, tq, ts, tz
         torch.cuda.empty_cache()
     return 0
