@@ -1,6 +1,7 @@
 // Device-side building blocks shared by the GEMV kernels (w4_gemv.cu,
 // w4_gemv_sk.cu): PTX wrappers for mbarriers, bulk copies and programmatic
-// dependent launch, the nibble-to-bf16 conversion and the tensor-core step.
+// dependent launch, the nibble-to-bf16 / -fp16 conversions and the
+// tensor-core steps.
 // Internal to libw4.
 #pragma once
 
@@ -267,7 +268,7 @@ __device__ __forceinline__ GroupData read_group(const unsigned char *st, int war
 
 // This lane's B registers for one group: the x pairs 8tq .. 8tq+7 of each of
 // the group's two 64-k chunks (xg points at word 8tq of the group's first
-// chunk of one token row, or at a zero patch).
+// chunk of the lane's token row).
 struct GroupB {
     uint4 b0l, b0h, b1l, b1h;
 };

@@ -21,18 +21,26 @@
 // LLM Inference Runtime ...", section "Bug #1", applied to weight streaming.
 //
 // Per consumer warp and group.  The 16-byte piece a lane owns in each 64-k
-// chunk holds four k-steps of its tensor-core A fragment.  Each word becomes
-// the four bf16x2 A registers without a conversion instruction:
-// (word >> 4p) & 0x000F000F | 0x43004300 is the bf16 pair (128 + q_even,
-// 128 + q_odd) exactly (bf16 has 7 fraction bits, so 128 + q is exact for
-// q < 128), and one bf16x2 fma adding -(128 + z) leaves q - z exactly.
-// mma.m16n8k16 (bf16 inputs, fp32 accumulation) multiplies the 16 x 16
-// weight block with up to 8 token columns of x; the products (q - z) * x are
-// exact, and the group scale is applied once per group in fp32:
-// acc += s * sum_group (q - z) x.  Lanes whose token column is >= M feed
-// zeros.  The launch shape depends only on K and N, so the result for one
-// token does not depend on M or on the other tokens (batch invariance,
-// "qengine", section "How it works").
+// chunk holds four k-steps of its tensor-core A fragment, and each word
+// becomes A registers without a conversion instruction.  Exact operand:
+// (word >> 4p) & 0x000F000F | 0x43004300 is the bf16 pair (128 + q, 128 + q')
+// exactly (bf16 has 7 fraction bits), and one bf16x2 fma adding -(128 + z)
+// leaves q - z exactly; mma.m16n8k16 (bf16, fp32 accumulation) multiplies
+// the 16 x 16 weight block with up to 8 token columns of x, the products
+// (q - z) * x are exact, and acc += s * sum_group (q - z) x.  Folded (blocks
+// of at least kFoldMinGroups groups): word & 0x000F000F and word & 0x00F000F0
+// (and the same of word >> 8) OR 0x64006400 are the fp16 pairs (1024 + q) and
+// (1024 + 16 q) exactly, one shift per word; x enters as fp16 scaled per
+// token by a power of two, and the zero point is removed once per group and
+// output through the group's half sums of x (group_mma_half_folded).  Token
+// columns >= M read token 0's row and are never stored.
+//
+// Batch invariance ("qengine", section "How it works"): the K split and the
+// arithmetic depend on K, N and the SM count only.  What else depends on M
+// -- shared-memory residency, the persistent grid of several-wave products
+// (one block per slot taking row blocks in turn), which of two x prologues
+// runs -- changes who computes a tile, not how, so a token's result is the
+// same for any M and any other tokens.
 //
 // Waits are bounded: a wait that exceeds ~2 s of clock cycles gives up, the
 // block records the failure in the header's kernel_error word and skips the
