@@ -323,15 +323,29 @@ w4_status w4_quantize(const uint16_t *w, int K, int N, int mode, uint32_t *qweig
  * The launch shape w4_gemv uses for an N x K weight on the current device:
  * 16-row tiles per thread block, the number of K splits (thread blocks of
  * one cluster that each reduce a slice of K and combine in a fixed order),
- * and whether the zero point is folded out of the inner product (1: each
- * group computes sum (128 + q) x - (128 + z) sum x in fp32, chosen when a
- * block streams at least 8 groups; 0: the tensor-core operand is q - z,
- * exactly).  Both are the same sum up to fp32 rounding.  Depends on K and N
- * only, never on M.  Outputs may be NULL.
+ * and whether the zero point is folded out of the inner product (1: fp16
+ * operands 1024 + q and 1024 + 16 q with x scaled per token into fp16
+ * range, the zero point removed once per group and output through the
+ * group's half sums of x, chosen when a block streams at least 8 groups;
+ * 0: the bf16 tensor-core operand is q - z, exactly).  Both are the same sum
+ * up to fp32 rounding.  Depends on K and N only, never on M.  Outputs may be
+ * NULL.
  * Errors: W4_ERR_INVALID_ARG, W4_ERR_CUDA (no device).
  */
 w4_status w4_gemv_config(int K, int N, int *tiles_per_block, int *k_splits,
                          int *zero_point_folded);
+
+/*
+ * Diagnostic with no counterpart in the pages: runs, in one thread of one
+ * block, the bounded mbarrier wait the GEMV kernels use on a barrier that
+ * nothing ever completes, and stores into *status (device, 4-byte aligned)
+ * 1 if the wait gave up after its limit (about 2 s of clock cycles, the
+ * expected outcome) or 0 if it wrongly returned success.  Shows on a real
+ * GPU that a wait which can never finish ends, reports, and leaves the
+ * context usable.  Asynchronous on `stream`; takes about 2 s on the GPU.
+ * Errors: W4_ERR_INVALID_ARG (status NULL or misaligned), W4_ERR_CUDA.
+ */
+w4_status w4_selftest_bounded_wait(uint32_t *status, w4_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -58,6 +58,7 @@ _gemv_swiglu = _decl("w4_gemv_swiglu", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_swiglu_f32 = _decl("w4_gemv_swiglu_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _quantize = _decl("w4_quantize", _ST, _P, _I, _I, _I, _P, _P, _P, _P)
 _gemv_ws_static = _decl("w4_gemv_ws_static", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
+_selftest_bounded_wait = _decl("w4_selftest_bounded_wait", _ST, _P, _P)
 _gemm = _decl("w4_gemm", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemm_f32 = _decl("w4_gemm_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_config = _decl("w4_gemv_config", _ST, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
@@ -256,6 +257,14 @@ def quantize(w, K: int, N: int, mode: int, qweight, scales, zeros, stream=None) 
     """w4_quantize: binary16 W [N, K] -> canonical qweight, scales, zeros."""
     _ok(_quantize(_ptr(w), K, N, int(mode), _ptr(qweight), _ptr(scales), _ptr(zeros),
                   _stream(stream, w)), "w4_quantize")
+
+
+def selftest_bounded_wait(status, stream=None) -> None:
+    """w4_selftest_bounded_wait: the GEMV kernels' bounded mbarrier wait on a
+    barrier nothing completes; `status` (a one-element int32 CUDA tensor)
+    becomes 1 when the wait gave up as it must.  About 2 s on the GPU."""
+    _ok(_selftest_bounded_wait(_ptr(status), _stream(stream, status)),
+        "w4_selftest_bounded_wait")
 
 
 def gemv_config(K: int, N: int):

@@ -126,3 +126,11 @@ def test_check_header(lib, mut, want):
     lib.w4_check_header.argtypes = [P, ctypes.c_int, ctypes.c_int]
     assert lib.w4_check_header(ctypes.cast(buf, P), 384, 64) == want
     assert lib.w4_check_header(None, 384, 64) == 1
+
+
+def test_selftest_argument_errors(lib):
+    lib.w4_selftest_bounded_wait.restype = ctypes.c_int
+    lib.w4_selftest_bounded_wait.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.w4_selftest_bounded_wait(None, None) == 1           # INVALID_ARG
+    assert lib.w4_selftest_bounded_wait(0x1002, None) == 1         # not 4-byte aligned
+
