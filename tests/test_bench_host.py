@@ -19,6 +19,14 @@ def test_chain_bytes_matches_layer_shapes():
     assert abs(bench.chain_bytes() / 1e9 - 3.420) < 0.001
 
 
+def test_small_chain_shapes_and_bytes():
+    # 0.5B shape: hidden 896, intermediate 4864, 14 query + 2 key/value heads of 64
+    assert syn.LAYER_05B == [("qkv", 896, (14 + 2 * 2) * 64), ("o", 896, 896),
+                             ("gate_up", 896, 2 * 4864), ("down", 4864, 896)]
+    per_layer = sum(bench.canonical_bytes(1, K, N) for _, K, N in syn.LAYER_05B)
+    assert syn.LAYERS_05B * per_layer == 188270592     # the bytes per step it reports
+
+
 def test_traffic_record_is_consistent():
     with open(os.path.join(bench.ROOT, "profiles", "gemv_traffic.json")) as f:
         rec = json.load(f)
