@@ -145,8 +145,11 @@ w4_status w4_dequant(const uint32_t *qweight, const uint16_t *scales,
  * with w4_check_header.  Every wait inside the kernel is bounded: a block that
  * gives up (about 2 s without progress -- never in normal operation) sets the
  * header's error word, which w4_check_header then reports, and leaves its
- * outputs unwritten.  Weights, scales and zeros must not be written by work
- * still running on the device when w4_gemv is enqueued.
+ * outputs unwritten.  So although qweight is passed as const, its buffer must
+ * be writable device memory: the kernel may write that one 32-bit word of the
+ * header (byte offset 28) and nothing else of it.  Weights, scales and zeros
+ * must not be written by work still running on the device when w4_gemv is
+ * enqueued.  The kernel writes no memory beyond y except that error word.
  * Errors: W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED (M outside 1..8), W4_ERR_CUDA.
  */
 w4_status w4_gemv(const void *qweight, const void *scales, const void *zeros,
@@ -334,6 +337,34 @@ w4_status w4_quantize(const uint16_t *w, int K, int N, int mode, uint32_t *qweig
  */
 w4_status w4_gemv_config(int K, int N, int *tiles_per_block, int *k_splits,
                          int *zero_point_folded);
+
+/* How w4_gemv launches a product (filled by w4_gemv_plan). */
+typedef struct w4_gemv_launch_info {
+    int k_splits;            /* thread blocks per cluster, each reducing a slice of K */
+    int zero_point_folded;   /* 1: fp16 operands, zero point folded out; 0: exact q - z */
+    int grid_x, grid_y;      /* launch grid: row blocks (or persistent slots) x K splits */
+    int persistent;          /* 1: each block takes row blocks in turn */
+    int overlap;             /* 1: launched with programmatic dependent launch (starts
+                                while the previous kernel in the stream finishes) */
+    int capped;              /* 1: shared memory padded so that at most the needed
+                                number of blocks share an SM */
+    int ring_stages;         /* depth of the shared-memory weight ring */
+    int wide_prologue;       /* 1: folded x prologue spread over (group, token) pairs */
+    int blocks_per_sm_max;   /* blocks per SM the kernel instance is built for */
+    size_t smem_bytes;       /* dynamic shared memory per block */
+} w4_gemv_launch_info;
+
+/*
+ * Diagnostic with no counterpart in the pages: the launch w4_gemv makes for
+ * M tokens of an N x K weight on the current device (split, arithmetic, grid,
+ * residency, overlap), so that callers and tests can see which kernel path a
+ * shape takes.  Computes the same plan w4_gemv computes before each launch;
+ * launches nothing.
+ *   info : host, written on success
+ * Errors: W4_ERR_INVALID_ARG (bad K/N, NULL info), W4_ERR_UNSUPPORTED (M
+ * outside 1..8, or no launch shape fits), W4_ERR_CUDA (no device).
+ */
+w4_status w4_gemv_plan(int M, int K, int N, w4_gemv_launch_info *info);
 
 /*
  * Diagnostic with no counterpart in the pages: runs, in one thread of one

@@ -2,6 +2,8 @@
 // then the launches.  Nothing here allocates device or pinned memory.
 #include <string.h>
 
+#include <atomic>
+
 #include "w4_internal.cuh"
 
 namespace {
@@ -12,15 +14,21 @@ bool valid_kn(int K, int N) { return K > 0 && K % w4::kGroup == 0 && N > 0; }
 
 w4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W4_OK : W4_ERR_CUDA; }
 
+// SM count of the current device, cached per device.  The cache entries are
+// atomic: host threads that race on a first call both read the attribute and
+// store the same value.
 int device_sms() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    if (dev >= 0 && dev < 64) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return -1;
-    if (dev >= 0 && dev < 64) cached[dev] = sms;
+    if (dev >= 0 && dev < 64) cached[dev].store(sms, std::memory_order_relaxed);
     return sms;
 }
 
@@ -271,6 +279,30 @@ w4_status w4_gemv_config(int K, int N, int *tiles_per_block, int *k_splits,
     if (tiles_per_block) *tiles_per_block = shape.warps;
     if (k_splits) *k_splits = shape.splits;
     if (zero_point_folded) *zero_point_folded = shape.fold ? 1 : 0;
+    return W4_OK;
+}
+
+w4_status w4_gemv_plan(int M, int K, int N, w4_gemv_launch_info *info) {
+    if (!valid_kn(K, N) || !info) return W4_ERR_INVALID_ARG;
+    if (M < 1 || M > W4_MAX_TOKENS) return W4_ERR_UNSUPPORTED;
+    const int sms = device_sms();
+    if (sms <= 0) return W4_ERR_CUDA;
+    w4::GemvShape shape;
+    if (!w4::gemv_shape(K, N, sms, &shape)) return W4_ERR_UNSUPPORTED;
+    w4::GemvLaunch L;
+    if (w4::plan_gemv(false, M, K, N, shape, sms, &L) != cudaSuccess) return W4_ERR_CUDA;
+    memset(info, 0, sizeof *info);
+    info->k_splits = shape.splits;
+    info->zero_point_folded = shape.fold ? 1 : 0;
+    info->grid_x = (int)L.grid.x;
+    info->grid_y = (int)L.grid.y;
+    info->persistent = L.persistent ? 1 : 0;
+    info->overlap = L.overlap ? 1 : 0;
+    info->capped = L.capped ? 1 : 0;
+    info->ring_stages = L.stages;
+    info->wide_prologue = L.arith == 2 ? 1 : 0;
+    info->blocks_per_sm_max = L.variant == 0 ? 2 : 3;
+    info->smem_bytes = L.smem_bytes;
     return W4_OK;
 }
 

@@ -49,6 +49,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -67,8 +68,8 @@ constexpr size_t kBlockSmemBudget = 113 * 1024;     // two blocks per SM
 constexpr size_t kBlockSmemBudget3 = 74 * 1024;     // three blocks per SM
 constexpr int kFoldMinGroups = 8;                   // see gemv_shape
 constexpr size_t kOverlapBelowBytes = 16u << 20;    // packed weights of a "short" product
-constexpr int kPersistMinTokens = 3;                // see launch_gemv
-constexpr int kWideMinTokens = 5;                   // see launch_gemv
+constexpr int kPersistMinTokens = 3;                // see plan_gemv
+constexpr int kWideMinTokens = 5;                   // see plan_gemv
 // Weight records a block requests before waiting for the previous kernel
 // (programmatic dependent launch); fewer than any ring holds, so that those
 // copies need no ring waits.
@@ -157,7 +158,7 @@ __device__ __forceinline__ void cluster_combine(float a0, float a1, float a2, fl
 // PERSIST (split S = 1 only): block c takes row blocks c, c + gridDim.x, ...
 // in turn through one ring and one x prologue; otherwise block (b, split)
 // takes row block b's K slice `split`.  WIDE (FOLD only): the x prologue's
-// work is spread over (group, token) pairs (see launch_gemv for its use).
+// work is spread over (group, token) pairs (see plan_gemv for its use).
 template <bool F32OUT, int MIN_BLOCKS, bool FOLD, int STAGES, bool PERSIST, bool WIDE>
 __global__ void __launch_bounds__(kThreads, MIN_BLOCKS)
 gemv_kernel(const char *__restrict__ qw, const char *__restrict__ sc,
@@ -694,7 +695,7 @@ bool gemv_shape(int K, int N, int num_sms, GemvShape *out) {
         if (smem_plan(K, S, W4_MAX_TOKENS, kStages).total > kBlockSmemBudget) continue;
         const long long ctas = (long long)NB * S;
         // A clustered grid counts as one wave only with 10% of the slots to
-        // spare, as in launch_gemv (beyond that it runs uncapped and slower).
+        // spare, as in plan_gemv (beyond that it runs uncapped and slower).
         const long long waves =
             S == 1 ? (ctas + slots - 1) / slots : (ctas * 11 + slots * 10 - 1) / (slots * 10);
         const long long cost = waves * ((G + S - 1) / S + fill);
@@ -775,10 +776,43 @@ int resident_blocks(const void *kern, size_t smem, int dev) {
 
 }  // namespace
 
-cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zeros,
-                        const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
-                        const GemvShape &shape, int swiglu_I, int num_sms,
-                        cudaStream_t stream) {
+namespace {
+
+using Kern = void (*)(const char *, const char *, const char *, const __nv_bfloat16 *, void *,
+                      uint32_t *, int, int, int, int, int, int, uint32_t, uint32_t);
+
+// [f32 out][variant][arithmetic][persistent]; variant 0: two blocks per SM,
+// 6 stages; 1: three, 6; 2: three, 5; arithmetic 0: exact q - z, 1: folded,
+// 2: folded with the wide x prologue
+#define W4_GEMV_KERNELS(F, MB, ST)                                                        \
+    {{gemv_kernel<F, MB, false, ST, false, false>, gemv_kernel<F, MB, false, ST, true, false>}, \
+     {gemv_kernel<F, MB, true, ST, false, false>, gemv_kernel<F, MB, true, ST, true, false>},   \
+     {gemv_kernel<F, MB, true, ST, false, true>, gemv_kernel<F, MB, true, ST, true, true>}}
+const Kern kKernels[2][3][3][2] = {
+    {W4_GEMV_KERNELS(false, 2, kStages), W4_GEMV_KERNELS(false, 3, kStages),
+     W4_GEMV_KERNELS(false, 3, kStagesShort)},
+    {W4_GEMV_KERNELS(true, 2, kStages), W4_GEMV_KERNELS(true, 3, kStages),
+     W4_GEMV_KERNELS(true, 3, kStagesShort)}};
+#undef W4_GEMV_KERNELS
+const int kVariantStages[3] = {kStages, kStages, kStagesShort};
+
+// Raise a kernel's dynamic shared memory limit to the device's opt-in
+// maximum, once per (kernel, device).  The flag is atomic: host threads that
+// race on a first call both set the attribute, which is idempotent.
+cudaError_t prepare_kernel(int f32_out, int v, int arith, int pers, int dev, int optin) {
+    static std::atomic<bool> done[2][3][3][2][64] = {};
+    std::atomic<bool> &flag = done[f32_out][v][arith][pers][dev];
+    if (flag.load(std::memory_order_acquire)) return cudaSuccess;
+    const cudaError_t r = cudaFuncSetAttribute(kKernels[f32_out][v][arith][pers],
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (r == cudaSuccess) flag.store(true, std::memory_order_release);
+    return r;
+}
+
+}  // namespace
+
+cudaError_t plan_gemv(bool f32_out, int M, int K, int N, const GemvShape &shape, int num_sms,
+                      GemvLaunch *out) {
     const int S = shape.splits;
     const long long blocks = (long long)row_blocks(N) * S;
     const int sms = num_sms > 0 ? num_sms : 1;
@@ -788,41 +822,20 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     const DeviceSmem &ds = device_smem(dev);
-    using Kern = void (*)(const char *, const char *, const char *, const __nv_bfloat16 *,
-                          void *, uint32_t *, int, int, int, int, int, int, uint32_t,
-                          uint32_t);
-    // [f32 out][variant][arithmetic][persistent]; variant 0: two blocks per
-    // SM, 6 stages; 1: three, 6; 2: three, 5; arithmetic 0: exact q - z,
-    // 1: folded, 2: folded with the wide x prologue
-#define W4_GEMV_KERNELS(F, MB, ST)                                                        \
-    {{gemv_kernel<F, MB, false, ST, false, false>, gemv_kernel<F, MB, false, ST, true, false>}, \
-     {gemv_kernel<F, MB, true, ST, false, false>, gemv_kernel<F, MB, true, ST, true, false>},   \
-     {gemv_kernel<F, MB, true, ST, false, true>, gemv_kernel<F, MB, true, ST, true, true>}}
-    static const Kern kKernels[2][3][3][2] = {
-        {W4_GEMV_KERNELS(false, 2, kStages), W4_GEMV_KERNELS(false, 3, kStages),
-         W4_GEMV_KERNELS(false, 3, kStagesShort)},
-        {W4_GEMV_KERNELS(true, 2, kStages), W4_GEMV_KERNELS(true, 3, kStages),
-         W4_GEMV_KERNELS(true, 3, kStagesShort)}};
-#undef W4_GEMV_KERNELS
-    static const int kVariantStages[3] = {kStages, kStages, kStagesShort};
-    static bool attr_done[2][3][3][2][64] = {};
     int arith = shape.fold ? 1 : 0;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)row_blocks(N), (unsigned)S, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    int na = 0;
+    cudaLaunchAttribute attr[1];
     if (S > 1) {
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = 1;
-        attr[na].val.clusterDim.y = (unsigned)S;
-        attr[na].val.clusterDim.z = 1;
-        ++na;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = (unsigned)S;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
     }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
 
     // Residency.  A grid of one wave runs as long as its most loaded SM, so
     // it should spread evenly: at most ceil(blocks / SMs) blocks per SM.
@@ -856,20 +869,10 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
             return 0;
         return want;
     };
-    auto prepare = [&](int v, int pers) -> cudaError_t {
-        const Kern kern = kKernels[f32_out][v][arith][pers];
-        if (!attr_done[f32_out][v][arith][pers][dev]) {
-            const cudaError_t r =
-                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ds.optin);
-            if (r != cudaSuccess) return r;
-            attr_done[f32_out][v][arith][pers][dev] = true;
-        }
-        return cudaSuccess;
-    };
     const int variant = smem_plan(K, S, M, kStages).total <= kBlockSmemBudget3        ? 1
                         : smem_plan(K, S, M, kStagesShort).total <= kBlockSmemBudget3 ? 2
                                                                                       : 0;
-    if ((e = prepare(variant, 0)) != cudaSuccess) return e;
+    if ((e = prepare_kernel(f32_out, variant, arith, 0, dev, ds.optin)) != cudaSuccess) return e;
     size_t smem_bytes = smem_plan(K, S, M, kVariantStages[variant]).total;
     bool capped = false;
     {
@@ -888,7 +891,8 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     // arithmetic of a row block is the same either way.
     int pers = 0;
     if (S == 1 && M >= kPersistMinTokens) {
-        if ((e = prepare(variant, 1)) != cudaSuccess) return e;
+        if ((e = prepare_kernel(f32_out, variant, arith, 1, dev, ds.optin)) != cudaSuccess)
+            return e;
         const int per_sm = resident_blocks((const void *)kKernels[f32_out][variant][arith][1],
                                            smem_bytes, dev);
         if (per_sm > 0 && blocks > (long long)per_sm * sms) {
@@ -902,24 +906,59 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
     // slot), the token-by-token prologue measured faster.
     if (arith == 1 && !pers && M >= kWideMinTokens) {
         arith = 2;
-        if ((e = prepare(variant, 0)) != cudaSuccess) return e;
+        if ((e = prepare_kernel(f32_out, variant, arith, 0, dev, ds.optin)) != cudaSuccess)
+            return e;
     }
-    const Kern kern = kKernels[f32_out][variant][arith][pers];
-    cfg.dynamicSmemBytes = smem_bytes;
-    const bool overlap = capped || (size_t)K * (size_t)N / 2 < kOverlapBelowBytes ||
-                         blocks > 3LL * sms;
-    if (overlap) {
+    out->shape = shape;
+    out->variant = variant;
+    out->arith = arith;
+    out->persistent = pers != 0;
+    out->capped = capped;
+    out->overlap = capped || (size_t)K * (size_t)N / 2 < kOverlapBelowBytes || blocks > 3LL * sms;
+    out->grid = cfg.gridDim;
+    out->smem_bytes = smem_bytes;
+    out->stages = kVariantStages[variant];
+    return cudaSuccess;
+}
+
+cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zeros,
+                        const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
+                        const GemvShape &shape, int swiglu_I, int num_sms,
+                        cudaStream_t stream) {
+    GemvLaunch L;
+    cudaError_t e = plan_gemv(f32_out, M, K, N, shape, num_sms, &L);
+    if (e != cudaSuccess) return e;
+    const int S = shape.splits;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = L.grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (S > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = (unsigned)S;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (L.overlap) {
         attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
-        cfg.numAttrs = na;
     }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    const Kern kern = kKernels[f32_out][L.variant][L.arith][L.persistent ? 1 : 0];
     const char *q = static_cast<const char *>(qweight);
+    // The kernel's one write outside y: the header's kernel-error word, set
+    // only when a wait inside the kernel gives up.
     uint32_t *err = reinterpret_cast<uint32_t *>(const_cast<char *>(q) + kErrorOffset);
     return cudaLaunchKernelEx(&cfg, kern, q, static_cast<const char *>(scales),
                               static_cast<const char *>(zeros),
                               reinterpret_cast<const __nv_bfloat16 *>(x), y, err, M, K, N, S,
-                              overlap ? kPreIssue : 0, swiglu_I, 0x000F000Fu,
+                              L.overlap ? kPreIssue : 0, swiglu_I, 0x000F000Fu,
                               shape.fold ? 0x64006400u : 0x43004300u);
 }
 

@@ -24,6 +24,8 @@
 // Workspace (device, 256-byte aligned, zero-filled before its first use): NB
 // counters (uint32, padded to 256 bytes), which every completed call leaves at
 // zero, then 2 * P partial slots of 4 KB (scratch, overwritten before read).
+#include <atomic>
+
 #include "w4_device.cuh"
 
 namespace w4 {
@@ -293,16 +295,19 @@ cudaError_t launch_gemv_ws(const void *qweight, const void *scales, const void *
                            void *workspace, int num_sms, cudaStream_t stream) {
     const int P = gemv_ws_blocks(K, N, num_sms);
     const SkPlan plan = sk_plan();
-    static bool attr_done[2][64] = {};
+    // Set once per (output type, device); atomic flags, so host threads that
+    // race on a first call both set the (idempotent) attribute.
+    static std::atomic<bool> attr_done[2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     auto kern = f32_out ? gemv_sk_kernel<true> : gemv_sk_kernel<false>;
-    if (dev < 64 && !attr_done[f32_out][dev]) {
+    if (!attr_done[f32_out][dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)plan.total);
         if (e != cudaSuccess) return e;
-        attr_done[f32_out][dev] = true;
+        attr_done[f32_out][dev].store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)P, 1, 1);

@@ -72,6 +72,23 @@ struct GemvShape {
 // shape fits the shared-memory budget.
 bool gemv_shape(int K, int N, int num_sms, GemvShape *out);
 
+// What launch_gemv will launch for (M, K, N): which kernel instance, the
+// grid, shared memory and whether it overlaps the previous kernel.
+struct GemvLaunch {
+    GemvShape shape;
+    int variant;        // 0: two blocks per SM, 6 stages; 1: three, 6; 2: three, 5
+    int arith;          // 0: exact q - z; 1: folded; 2: folded, wide x prologue
+    bool persistent;    // blocks take row blocks in turn
+    bool capped;        // shared memory padded to cap blocks per SM
+    bool overlap;       // programmatic dependent launch
+    dim3 grid;
+    size_t smem_bytes;
+    int stages;
+};
+
+cudaError_t plan_gemv(bool f32_out, int M, int K, int N, const GemvShape &shape, int num_sms,
+                      GemvLaunch *out);
+
 // swiglu_I = 0: y[M][N] = W x.  swiglu_I = I > 0: W is a gate/up-interleaved
 // weight of N = swiglu_rows(I) rows and y[M][I] = silu(gate x) * (up x).
 cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zeros,

@@ -63,6 +63,16 @@ _gemm = _decl("w4_gemm", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemm_f32 = _decl("w4_gemm_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_config = _decl("w4_gemv_config", _ST, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
                      ctypes.POINTER(_I))
+
+
+class _LaunchInfo(ctypes.Structure):
+    _fields_ = [("k_splits", _I), ("zero_point_folded", _I), ("grid_x", _I), ("grid_y", _I),
+                ("persistent", _I), ("overlap", _I), ("capped", _I), ("ring_stages", _I),
+                ("wide_prologue", _I), ("blocks_per_sm_max", _I),
+                ("smem_bytes", ctypes.c_size_t)]
+
+
+_gemv_plan = _decl("w4_gemv_plan", _ST, _I, _I, _I, ctypes.POINTER(_LaunchInfo))
 _gemv_workspace_bytes = _decl("w4_gemv_workspace_bytes", _ST, _I, _I,
                               ctypes.POINTER(ctypes.c_size_t))
 _gemv_ws = _decl("w4_gemv_ws", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P, ctypes.c_size_t, _P)
@@ -273,6 +283,16 @@ def gemv_config(K: int, N: int):
     t, s, f = _I(), _I(), _I()
     _ok(_gemv_config(K, N, ctypes.byref(t), ctypes.byref(s), ctypes.byref(f)), "w4_gemv_config")
     return t.value, s.value, bool(f.value)
+
+
+def gemv_plan(M: int, K: int, N: int) -> dict:
+    """The launch w4_gemv makes for M tokens of an N x K weight on the current
+    device (w4_gemv_plan): split, arithmetic, grid, residency, overlap."""
+    info = _LaunchInfo()
+    _ok(_gemv_plan(M, K, N, ctypes.byref(info)), "w4_gemv_plan")
+    return {name: (bool(getattr(info, name)) if name in
+                   ("zero_point_folded", "persistent", "overlap", "capped", "wide_prologue")
+                   else int(getattr(info, name))) for name, _ in _LaunchInfo._fields_}
 
 
 @dataclass

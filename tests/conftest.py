@@ -27,3 +27,21 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    # How many GEMV outputs were more than one bf16 ulp from RNE(y_ref) (each
+    # inside the fp32 bound; see tests/w4_testutil.check_gemv).
+    try:
+        from tests import w4_testutil as tu
+    except Exception:
+        return
+    if not tu.OFF_ULP_STATS:
+        return
+    off = sum(o for _, o, _ in tu.OFF_ULP_STATS)
+    total = sum(n for _, _, n in tu.OFF_ULP_STATS)
+    worst = max(tu.OFF_ULP_STATS, key=lambda t: t[1] / max(t[2], 1))
+    terminalreporter.write_line(
+        f"bf16 outputs more than 1 ulp from RNE(y_ref): {off} of {total} compared "
+        f"in {len(tu.OFF_ULP_STATS)} GEMV checks (largest share: {worst[1]} of {worst[2]} "
+        f"in {worst[0]})")

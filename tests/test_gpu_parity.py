@@ -395,3 +395,35 @@ def test_ws_and_cluster_paths_agree(w4):
     n_ws = 8 + K // 128 + K // 128 + 1
     bound = 2.0 ** -23 * (n_cl * tu.folded_abs(p, rows) + n_ws * refabs)
     assert (np.abs(a32[:, rows].astype(np.float64) - b32[:, rows]) <= bound).all()
+
+
+# ---- nothing is written outside y ---------------------------------------------------
+
+@pytest.mark.parametrize("path,M,K,N", [("cluster", 1, 3584, 3584), ("cluster", 8, 18944, 200),
+                                        ("cluster", 1, 3584, 37888), ("cluster", 4, 1024, 64037),
+                                        ("ws", 3, 3584, 1000), ("swiglu", 2, 1024, 333)])
+def test_no_write_outside_y(w4, path, M, K, N):
+    """The output is written exactly: y sits between two 4 KB guard bands of a
+    sentinel pattern, which must be unchanged after bf16 and fp32 calls (the
+    cluster split at one-wave, tall-K and persistent launch shapes, the
+    workspace split, the SwiGLU product with a ragged last tile)."""
+    rows = 2 * N if path == "swiglu" else N
+    p = syn.make_problem(f"guard.{path}.{M}.{K}.{N}", K, rows, M, seed=16)
+    qw, sc, zp, x = tu.to_device(p)
+    packed = w4.pack_swiglu(qw, sc, zp, K, N) if path == "swiglu" else w4.pack(qw, sc, zp, K, N)
+    ws = w4.workspace(K, N) if path == "ws" else None
+    guard = 4096
+    for esize, fn in ((2, "gemv"), (4, "gemv_f32")):
+        nbytes = M * N * esize
+        buf = torch.full((2 * guard + nbytes,), 0x5A, dtype=torch.uint8, device="cuda")
+        y = buf[guard:guard + nbytes].view(torch.bfloat16 if esize == 2 else torch.float32)
+        y = y.view(M, N)
+        if path == "swiglu":
+            getattr(packed, fn)(x, y)
+        else:
+            getattr(packed, fn)(x, y, workspace=ws)
+        torch.cuda.synchronize()
+        host = buf.cpu().numpy()
+        assert (host[:guard] == 0x5A).all(), f"{path} {fn}: write before y"
+        assert (host[guard + nbytes:] == 0x5A).all(), f"{path} {fn}: write after y"
+        assert not (host[guard:guard + nbytes] == 0x5A).all(), f"{path} {fn}: y not written"
