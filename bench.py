@@ -152,7 +152,9 @@ class ClockSampler:
 
 class OracleSampler:
     """Runs the CPU oracle over the chain's GEMVs in chain order (layer 0 qkv,
-    o, gate_up, down, layer 1 ...), timing only the oracle call."""
+    o, gate_up, down, layer 1 ...), timing only the oracle call; also the
+    per-config CPU table and the check of the GPU chain's outputs (the one
+    place where the benchmark runs the oracle besides the reference arm)."""
 
     def __init__(self):
         self.pos = 0
@@ -177,11 +179,139 @@ class OracleSampler:
         return nbytes, spent, n
 
 
-def cpu_baseline(seconds: float = 10.0):
-    b, t, n = OracleSampler().run(seconds)
-    return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"first {n} GEMVs of the chain in order (layer 0 qkv, o, gate_up, "
-                      f"down, ...), M=1, single-threaded fp64 oracle, {t:.1f} s of compute"}
+    # Per-config CPU times: the workloads' GEMVs, one call each, on one core
+    # (the oracle) and on all host cores (the same loop with rows spread over
+    # OpenMP threads).
+    CONFIGS = [
+        ("cfg1 896x896 M=1", [("single.896x896", 896, 896)], 1),
+        ("cfg2 0.5B layer M=1 (4 GEMVs)", [(f"qwen0.5b.{k}", K, N) for k, K, N in syn.LAYER_05B], 1),
+        ("cfg3 7B layer M=1 (4 GEMVs)", [(f"qwen7b.{k}", K, N) for k, K, N in syn.LAYER_7B], 1),
+        ("cfg4 27B up+down M=1", [("27b.up", 5120, 17408), ("27b.down", 17408, 5120)], 1),
+        ("cfg4 27B up+down M=8 (all cores only)", [("27b.up", 5120, 17408),
+                                                   ("27b.down", 17408, 5120)], 8),
+        ("cfg5 LM head M=1", [("qwen7b.lm_head", 3584, 152064)], 1),
+    ]
+
+    def per_config(self):
+        import oracle
+        rows = []
+        w = syn.make_problem("cpu.warm", 256, 256, 1, SEED)   # start the thread pool
+        oracle.gemv_f64_omp(w.qweight, w.scales, w.zeros, w.x, 1, 256, 256)
+        for label, gemvs, M in self.CONFIGS:
+            one_core = "all cores only" not in label
+            t1 = tp = 0.0
+            nbytes = 0
+            for name, K, N in gemvs:
+                srange = (0.0005, 0.01) if name.startswith("27b") else SCALES
+                qw, sc, zp = syn.make_weights(f"cpu.{name}", K, N, SEED, srange)
+                x = syn.make_x(f"cpu.{name}.M{M}", M, K, SEED)
+                if one_core:
+                    t0 = time.perf_counter()
+                    oracle.gemv_f64(qw, sc, zp, x, M, K, N)
+                    t1 += time.perf_counter() - t0
+                t0 = time.perf_counter()
+                oracle.gemv_f64_omp(qw, sc, zp, x, M, K, N)
+                tp += time.perf_counter() - t0
+                nbytes += canonical_bytes(M, K, N)
+            row = {"config": label, "us_all_cores": round(tp * 1e6, 1),
+                   "GBps_all_cores": round(nbytes / tp / 1e9, 4)}
+            if one_core:
+                row.update({"us_1core": round(t1 * 1e6, 1),
+                            "GBps_1core": round(nbytes / t1 / 1e9, 4)})
+            rows.append(row)
+        return rows, oracle.omp_threads()
+
+    def omp_chain(self, seconds: float):
+        """The chain sample of run() with the OpenMP loop (all host cores)."""
+        import oracle
+        nbytes, spent, n = 0, 0.0, 0
+        pos = 0
+        while n == 0 or spent < seconds:
+            layer, j = divmod(pos, len(syn.LAYER_7B))
+            kind, K, N = syn.LAYER_7B[j]
+            pos = (pos + 1) % (syn.LAYERS_7B * len(syn.LAYER_7B))
+            qw, sc, zp = syn.make_weights(f"chain7b.L{layer}.{kind}", K, N, SEED, SCALES)
+            x = syn.make_x(f"chain7b.x.{kind}", 1, K, SEED)
+            t0 = time.perf_counter()
+            oracle.gemv_f64_omp(qw, sc, zp, x, 1, K, N)
+            spent += time.perf_counter() - t0
+            nbytes += canonical_bytes(1, K, N)
+            n += 1
+        return nbytes, spent, n
+
+    def check_outputs(self, ylast_bits, rows_per: int = 256):
+        """Correctness of the timed chain ("CodeAlign-Runtime", section
+        "Benchmarking Methodology": correctness accompanies speed): the last
+        layer's four bf16 outputs (bit patterns, read back after the timed
+        region) against the oracle on sampled rows -- the first and last 32
+        and a seeded random sample -- as ulps from the oracle's value rounded
+        to bf16, and the relative L2 error of the bf16 values (which includes
+        the bf16 rounding itself, about 2^-9 per value)."""
+        import oracle
+        layer = syn.LAYERS_7B - 1
+        rng = np.random.default_rng(SEED)
+        off, worst, n_gt1, n_all = 0, 0, 0, 0
+        num = den = 0.0
+        for kind, K, N in syn.LAYER_7B:
+            got = np.asarray(ylast_bits[off:off + N], np.uint16)
+            off += N
+            qw, sc, zp = syn.make_weights(f"chain7b.L{layer}.{kind}", K, N, SEED, SCALES)
+            x = syn.make_x(f"chain7b.x.{kind}", 1, K, SEED)
+            rows = np.unique(np.concatenate([np.arange(32), np.arange(N - 32, N),
+                                             rng.choice(N, rows_per, replace=False)]))
+            ref = oracle.gemv_rows_f64(qw, sc, zp, x, 1, K, N, rows)[0]
+            want = oracle.bf16_rne(ref.astype(np.float32))
+            g = got[rows].astype(np.int64)
+            w = want.astype(np.int64)
+            ordg = np.where(g & 0x8000, -(g & 0x7FFF), g)
+            ordw = np.where(w & 0x8000, -(w & 0x7FFF), w)
+            ulps = np.abs(ordg - ordw)
+            worst = max(worst, int(ulps.max()))
+            n_gt1 += int((ulps > 1).sum())
+            n_all += len(rows)
+            gv = (got[rows].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            num += float(((gv - ref) ** 2).sum())
+            den += float((ref ** 2).sum())
+        rel = (num / den) ** 0.5 if den > 0 else 0.0
+        return {"outputs_checked": n_all, "of": "last layer's qkv, o, gate_up, down (bf16)",
+                "max_ulp_from_rne_ref": worst, "outputs_gt_1ulp": n_gt1,
+                "rel_l2_bf16": round(rel, 6),
+                "pass": bool(n_gt1 <= 0.01 * n_all and rel <= 4e-3)}
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(seconds: float = 10.0, ylast_bits=None):
+    """The oracle on the host: the chain sample on one core (the baseline),
+    the same sample with the OpenMP loop on all cores, a per-config table,
+    and the correctness check of the GPU chain's last outputs."""
+    sampler = OracleSampler()
+    b, t, n = sampler.run(seconds)
+    out = {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"first {n} GEMVs of the chain in order (layer 0 qkv, o, gate_up, "
+                     f"down, ...), M=1, single-threaded fp64 oracle, {t:.1f} s of compute",
+           "cpu_model": cpu_model(), "host_cores": os.cpu_count()}
+    try:
+        bo, to, no = sampler.omp_chain(max(1.0, seconds / 4))
+        rows, threads = sampler.per_config()
+        out["all_cores"] = {"value": round(bo / to / 1e9, 4), "unit": "GB/s", "cores": threads,
+                            "kind": "oracle loop, OpenMP over output rows",
+                            "sample": f"first {no} GEMVs of the chain, {to:.1f} s"}
+        out["per_config"] = rows
+    except Exception as e:          # the OpenMP build is optional on a host without libgomp
+        out["all_cores"] = {"unavailable": str(e)[:200]}
+    correctness = sampler.check_outputs(ylast_bits) if ylast_bits is not None else None
+    return out, correctness
 
 
 # ---- distributed plumbing -----------------------------------------------------------------
@@ -376,9 +506,30 @@ def gpu_arm(args):
     value = job_gbps(world, bytes_step, ms)
     gu_bytes = canonical_bytes(1, 3584, 37888)
     achieved = gu_bytes / (gu_launch_us * 1e-6) / 1e9
+    ylast_bits = ylast.view(torch.int16).cpu().numpy().view(np.uint16).copy()
+    # after the timed regions: the read ceiling, then the per-call block
+    read_peak, read_ok = read_peak_gbs(w4, torch, dev, stream)
+    rpeak = max(read_peak.values())
+    per_shape = per_shape_block(w4, torch, dev, stream, packed, args.warmup, peak, rpeak) \
+        if not args.no_per_shape else []
     result = None
     if rank == 0:
         clk = clocks.summary()
+        # ideal step at the measured copy peak, and where the rest goes: per
+        # GEMV kind, 28 x (per-call time alone - its ideal); what remains is
+        # the cost of running the calls back to back in the graph
+        ideal_ms = bytes_step / (peak * 1e9) * 1e3
+        split = {"ideal_ms": round(ideal_ms, 4)}
+        alone = 0.0
+        for kind, K, N in syn.LAYER_7B:
+            rec = [r for r in per_shape if r["shape"] == f"qwen7b.{kind}" and r["M"] == 1]
+            if rec:
+                ideal_us = canonical_bytes(1, K, N) / (peak * 1e3)
+                split[f"{kind}_excess_ms"] = round(syn.LAYERS_7B * (rec[0]["us"] - ideal_us) / 1e3,
+                                                   4)
+                alone += syn.LAYERS_7B * rec[0]["us"] / 1e3
+        if per_shape:
+            split["chaining_ms"] = round(ms - alone, 4)
         result = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -397,7 +548,12 @@ def gpu_arm(args):
                          "traffic": gemv_traffic(),
                          "kernel": "w4 gemv, gate_up 3584->37888, M=1",
                          "bytes_per_launch": gu_bytes,
-                         "launch_us": round(gu_launch_us, 3), "peak_kind": peak_kind},
+                         "launch_us": round(gu_launch_us, 3), "peak_kind": peak_kind,
+                         "read_peak": rpeak, "frac_of_read_peak": round(achieved / rpeak, 4)},
+            "read_peak_gbs": dict(read_peak, measured_ok=read_ok,
+                                  how="w4_stream_read over a 4 GiB buffer, best of 5"),
+            "ideal_vs_actual": split,
+            "per_shape": per_shape,
             "e2e": {"value": round(job_gbps(world, bytes_step, e2e_ms), 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms, 5), "host_ms_per_step": round(1e3 * t_host, 5)},
@@ -409,18 +565,123 @@ def gpu_arm(args):
         dist.destroy_process_group()
     if rank == 0:
         if not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+            result["cpu_baseline"], result["correctness"] = cpu_baseline(args.cpu_seconds,
+                                                                         ylast_bits)
         print(json.dumps(result), flush=True)
     return 0
 
 
+def time_rotating(w4, torch, stream, base, x, y, l2, warmup, replays=25, max_copies=4096):
+    """Per-call device time of base.gemv(x, y): R calls over rotating copies
+    of the weight (together > 3 x L2, so no call finds its weight in L2)
+    captured in one CUDA graph, the graph replayed `replays` times after
+    `warmup` replays; per-call time = replay time / R.  Returns (median, mean,
+    p90, p99) in us, the number of copies and R."""
+    qb, sb, zb = base.qweight.numel(), base.scales.numel(), base.zeros.numel()
+    copies = min(max_copies, max(2, -(-3 * l2 // (qb + sb + zb)) + 1))
+    packs = [base] + [w4.PackedWeight(base.K, base.N, base.qweight.clone(), base.scales.clone(),
+                                      base.zeros.clone()) for _ in range(copies - 1)]
+    reps = max(1, -(-64 // copies)) * copies
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for pw in packs[:2]:
+            pw.gemv(x, y, stream=stream)
+    stream.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(reps):
+            packs[i % copies].gemv(x, y, stream=stream)
+    times = []
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+        for _ in range(replays):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / reps)
+    del packs, g
+    pct = np.percentile(times, [90, 99])
+    return (statistics.median(times), statistics.fmean(times), float(pct[0]), float(pct[1]),
+            copies, reps)
+
+
+# The per-call block of the default line: the 7B layer's GEMVs and the LM head
+# at one and eight tokens (the shapes the 80 % target is stated for).
+PER_SHAPE_DEFAULT = [("qwen7b.qkv", 3584, 4608), ("qwen7b.o", 3584, 3584),
+                     ("qwen7b.gate_up", 3584, 37888), ("qwen7b.down", 18944, 3584),
+                     ("qwen7b.lm_head", 3584, 152064)]
+
+
+def per_shape_block(w4, torch, dev, stream, chain_packed, warmup, peak, read_peak):
+    """Per-call timing (time_rotating) of PER_SHAPE_DEFAULT at M = 1 and 8;
+    the 7B shapes reuse the chain's layer-0 weights, the LM head is drawn
+    here."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    layer0 = {kind: pw for kind, pw in chain_packed[:len(syn.LAYER_7B)]}
+    out = []
+    for name, K, N in PER_SHAPE_DEFAULT:
+        kind = name.split(".", 1)[1]
+        if kind in layer0:
+            base = layer0[kind]
+        else:
+            qw, sc, zp = syn.make_weights(name, K, N, SEED, SCALES)
+            base = w4.pack(torch.from_numpy(qw.view(np.int32)).to(dev),
+                           torch.from_numpy(sc.view(np.int16)).to(dev),
+                           torch.from_numpy(zp).to(dev), K, N)
+        for M in (1, 8):
+            x = torch.from_numpy(syn.make_x(f"{name}.M{M}", M, K, SEED).view(np.int16)) \
+                .to(dev).view(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            med, mean, p90, p99, copies, reps = time_rotating(w4, torch, stream, base, x, y, l2,
+                                                              warmup)
+            b = canonical_bytes(M, K, N)
+            gbps = b / med / 1e3
+            out.append({"shape": name, "M": M, "K": K, "N": N, "us": round(med, 3),
+                        "GBps": round(gbps, 1), "frac_of_peak": round(gbps / peak, 4),
+                        "frac_of_read_peak": round(gbps / read_peak, 4) if read_peak else None,
+                        "p99_us": round(p99, 3), "copies": copies, "calls_per_graph": reps})
+        del base
+        torch.cuda.empty_cache()
+    return out
+
+
+def read_peak_gbs(w4, torch, dev, stream, gib: int = 4):
+    """The read-only ceiling measured with the library's own streaming kernel
+    (w4_stream_read): a `gib` GiB buffer (far above L2) read once per call,
+    best of 5 after 2 warm-up calls, for the bulk-copy ring (the GEMV's method)
+    and for 128-bit loads."""
+    buf = torch.empty(gib << 30, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(2, dtype=torch.int32, device=dev)
+    res = {}
+    for mode, label in ((w4.STREAM_READ_RING, "bulk_copy_ring"), (w4.STREAM_READ_LD128, "ld128")):
+        best = None
+        with torch.cuda.stream(stream):
+            for i in range(7):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                w4.stream_read(buf, mode, sink, stream=stream)
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 2:
+                    ms = e0.elapsed_time(e1)
+                    best = ms if best is None else min(best, ms)
+        res[label] = round(buf.numel() / (best * 1e-3) / 1e9, 1)
+    ok = int(sink[1].item()) == 0
+    del buf
+    torch.cuda.empty_cache()
+    return res, ok
+
+
 def per_shape_arm(args):
-    """Per-call timing of every workload shape: R calls over rotating weight
-    copies (so that the weights never sit in L2) captured in one CUDA graph,
-    the graph replayed 25 times after the warm-up; per-call time = replay
-    time / R, reported as the median (and mean, p90, p99, and a flag when
-    the mean is more than 15 % above the median).  The shapes run in a
-    shuffled (seeded) order.  Prints one JSON line per (shape, M)."""
+    """Per-call timing of every workload shape (time_rotating: R calls over
+    rotating weight copies in one CUDA graph, replayed 25 times after the
+    warm-up; median per call, with mean, p90, p99 and a flag when the mean is
+    more than 15 % above the median).  The shapes run in a shuffled (seeded)
+    order.  Prints one JSON line per (shape, M)."""
     import torch
 
     from int4_weight_only_w4_gb300 import w4
@@ -433,52 +694,24 @@ def per_shape_arm(args):
     stream = torch.cuda.Stream(device=dev)
     for name in names:
         _, K, N, Ms, srange = syn.shape(name)
-        qb, sb, zb = w4.repacked_sizes(K, N)
-        copies = min(4096, max(2, -(-3 * l2 // (qb + sb + zb)) + 1))
-        if args.kernel_case:
-            copies = 1                      # one weight, for profiler captures
         qw, sc, zp = syn.make_weights(name, K, N, SEED, srange)
-        tq = torch.from_numpy(qw.view(np.int32)).to(dev)
-        ts = torch.from_numpy(sc.view(np.int16)).to(dev)
-        tz = torch.from_numpy(zp).to(dev)
-        base = w4.pack(tq, ts, tz, K, N)
-        packs = [base] + [w4.PackedWeight(K, N, base.qweight.clone(), base.scales.clone(),
-                                          base.zeros.clone()) for _ in range(copies - 1)]
+        base = w4.pack(torch.from_numpy(qw.view(np.int32)).to(dev),
+                       torch.from_numpy(sc.view(np.int16)).to(dev),
+                       torch.from_numpy(zp).to(dev), K, N)
         for M in Ms:
             x = torch.from_numpy(syn.make_x(f"{name}.M{M}", M, K, SEED).view(np.int16)) \
                 .to(dev).view(torch.bfloat16)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             if args.kernel_case:
+                # one weight, eager calls only: the case a profiler captures
                 with torch.cuda.stream(stream):
                     for _ in range(args.warmup + args.steps):
                         base.gemv(x, y, stream=stream)
                 stream.synchronize()
                 print(json.dumps({"kernel_case": name, "M": M, "K": K, "N": N}), flush=True)
                 continue
-            reps = max(1, -(-64 // copies)) * copies
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                for pw in packs[:2]:
-                    pw.gemv(x, y, stream=stream)
-            stream.synchronize()
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(reps):
-                    packs[i % copies].gemv(x, y, stream=stream)
-            times = []
-            with torch.cuda.stream(stream):
-                for _ in range(args.warmup):
-                    g.replay()
-                for _ in range(25):
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    g.replay()
-                    e1.record(stream)
-                    e1.synchronize()
-                    times.append(e0.elapsed_time(e1) * 1e3 / reps)
-            us = statistics.median(times)
-            mean = statistics.fmean(times)
-            pct = np.percentile(times, [90, 99])
+            us, mean, p90, p99, copies, reps = time_rotating(w4, torch, stream, base, x, y, l2,
+                                                             args.warmup)
             # eager single call (includes launch overhead through the binding)
             t0 = time.perf_counter()
             for _ in range(20):
@@ -492,11 +725,11 @@ def per_shape_arm(args):
                               "peak_kind": peak_kind, "bytes": b, "copies": copies,
                               "calls_per_graph": reps, "splits": w4.gemv_config(K, N)[1],
                               "eager_us_per_call": round(eager_us, 2),
-                              "mean_us": round(mean, 3), "p90_us": round(float(pct[0]), 3),
-                              "p99_us": round(float(pct[1]), 3),
+                              "mean_us": round(mean, 3), "p90_us": round(p90, 3),
+                              "p99_us": round(p99, 3),
                               "mean_above_median_15pct": mean > 1.15 * us,
-                              "replays": len(times)}), flush=True)
-        del packs, base, tq, ts, tz
+                              "replays": 25}), flush=True)
+        del base
         torch.cuda.empty_cache()
     return 0
 
@@ -780,6 +1013,8 @@ def main():
     ap.add_argument("--impl", choices=["w4", "reference"], default="w4")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-shape", action="store_true",
+                    help="leave the per-call block out of the default line")
     ap.add_argument("--gemm", action="store_true",
                     help="per-call timing of w4_gemm (M > 8, passes of 8 tokens)")
     ap.add_argument("--swiglu", action="store_true",

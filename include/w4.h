@@ -244,7 +244,13 @@ w4_status w4_gemv_ws_f32(const void *qweight, const void *scales, const void *ze
  * on the GPU (other streams, other host threads) race and give wrong results.
  * A product needs w4_gemv_workspace_bytes(K, N) bytes of scratch; more than
  * W4_STATIC_SCRATCH_BYTES is refused with W4_ERR_SCRATCH_LIMIT before
- * anything else is checked or enqueued.
+ * anything else is checked or enqueued.  That need depends on the SM count:
+ * with NB = ceil(N / 128) row blocks and W = NB * K / 128 records, it is
+ * round_up(4 * NB, 256) bytes of counters plus 2 * min(W, 3 * SMs) * 4096
+ * bytes of partial sums.  On a 152-SM GB300 the partial sums take at most
+ * 3.56 MiB, which leaves room for about 114,000 row blocks (14.6 M output
+ * rows); on a GPU with 171 or more SMs the partial sums alone exceed the
+ * array for every product of at least 3 * SMs records.
  * Errors: W4_ERR_SCRATCH_LIMIT, W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED (M
  * outside 1..8), W4_ERR_CUDA (no device, or the array could not be found).
  */
@@ -377,6 +383,30 @@ w4_status w4_gemv_plan(int M, int K, int N, w4_gemv_launch_info *info);
  * Errors: W4_ERR_INVALID_ARG (status NULL or misaligned), W4_ERR_CUDA.
  */
 w4_status w4_selftest_bounded_wait(uint32_t *status, w4_stream_t stream);
+
+/* Modes of w4_stream_read. */
+#define W4_STREAM_READ_RING 0
+#define W4_STREAM_READ_LD128 1
+
+/*
+ * Diagnostic: reads `bytes` of device memory once and folds them into one
+ * word, to measure the read-only bandwidth a kernel gets on this GPU -- the
+ * ceiling a memory-bound GEMV is judged against ("qengine", section
+ * "Learnings": measure your own ceiling with a plain read benchmark; a copy
+ * also writes, and the data sheet is a peak no kernel reaches).
+ *   W4_STREAM_READ_RING : the GEMV's own method -- contiguous shares of the
+ *     buffer moved in 8 KB cp.async.bulk records through a 12-stage
+ *     shared-memory ring, two blocks per SM; `bytes` a multiple of 8192.
+ *   W4_STREAM_READ_LD128: 16-byte streaming loads in a grid-stride loop, four
+ *     blocks of 512 threads per SM; `bytes` a multiple of 16.
+ *   src : device, 16-byte aligned
+ *   out : device uint32 [2]; out[0] is xor-ed with the folded word, out[1]
+ *         gets bit 0 if a bounded wait gave up (never in normal operation)
+ * Asynchronous on `stream`; time it with events around the call.
+ * Errors: W4_ERR_INVALID_ARG (pointers, alignment, size, mode), W4_ERR_CUDA.
+ */
+w4_status w4_stream_read(const void *src, size_t bytes, int mode, uint32_t *out,
+                         w4_stream_t stream);
 
 #ifdef __cplusplus
 }

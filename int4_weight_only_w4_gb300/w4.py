@@ -59,6 +59,7 @@ _gemv_swiglu_f32 = _decl("w4_gemv_swiglu_f32", _ST, _P, _P, _P, _P, _P, _I, _I, 
 _quantize = _decl("w4_quantize", _ST, _P, _I, _I, _I, _P, _P, _P, _P)
 _gemv_ws_static = _decl("w4_gemv_ws_static", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _selftest_bounded_wait = _decl("w4_selftest_bounded_wait", _ST, _P, _P)
+_stream_read = _decl("w4_stream_read", _ST, _P, ctypes.c_size_t, _I, _P, _P)
 _gemm = _decl("w4_gemm", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemm_f32 = _decl("w4_gemm_f32", _ST, _P, _P, _P, _P, _P, _I, _I, _I, _P)
 _gemv_config = _decl("w4_gemv_config", _ST, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
@@ -275,6 +276,18 @@ def selftest_bounded_wait(status, stream=None) -> None:
     becomes 1 when the wait gave up as it must.  About 2 s on the GPU."""
     _ok(_selftest_bounded_wait(_ptr(status), _stream(stream, status)),
         "w4_selftest_bounded_wait")
+
+
+STREAM_READ_RING = 0      # W4_STREAM_READ_RING
+STREAM_READ_LD128 = 1     # W4_STREAM_READ_LD128
+
+
+def stream_read(src, mode: int, out, stream=None) -> None:
+    """w4_stream_read: read all of `src` (a CUDA tensor) once, folding it
+    into out[0] (out: two-element int32 CUDA tensor); for measuring the
+    read-only bandwidth."""
+    _ok(_stream_read(_ptr(src), src.numel() * src.element_size(), int(mode), _ptr(out),
+                     _stream(stream, src)), "w4_stream_read")
 
 
 def gemv_config(K: int, N: int):

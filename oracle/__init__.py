@@ -26,6 +26,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "w4_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libw4oracle.so")
 _lib = None
+_OMP_SRC = os.path.join(_HERE, "w4_cpu_omp.c")
+_OMP_PATH = os.path.join(_HERE, "libw4cpu_omp.so")
+_omp = None
 
 GROUP = 128
 
@@ -42,6 +45,49 @@ def build(force: bool = False) -> str:
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
+
+
+def build_omp(force: bool = False) -> str:
+    """Compile the OpenMP CPU baseline (w4_cpu_omp.c) into libw4cpu_omp.so."""
+    if (not force and os.path.exists(_OMP_PATH)
+            and os.path.getmtime(_OMP_PATH) >= os.path.getmtime(_OMP_SRC)):
+        return _OMP_PATH
+    tmp = _OMP_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", "-o", tmp, _OMP_SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _OMP_PATH)
+    return _OMP_PATH
+
+
+def _load_omp():
+    global _omp
+    if _omp is None:
+        lib = ctypes.CDLL(build_omp())
+        lib.w4c_threads.restype = ctypes.c_int
+        lib.w4c_threads.argtypes = []
+        lib.w4c_gemv_f64.restype = None
+        lib.w4c_gemv_f64.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+        _omp = lib
+    return _omp
+
+
+def omp_threads() -> int:
+    """Threads the OpenMP CPU baseline uses (all host cores unless limited)."""
+    return int(_load_omp().w4c_threads())
+
+
+def gemv_f64_omp(qweight, scales, zeros, x, M: int, K: int, N: int):
+    """The same y[M, N] as gemv_f64, computed with the rows spread over all
+    host cores (CPU baseline for timing; bit-identical to gemv_f64)."""
+    qweight, scales, zeros = _check(qweight, scales, zeros, K, N)
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    if x.shape != (M, K):
+        raise ValueError("x must be [M, K]")
+    y = np.empty((M, N), dtype=np.float64)
+    _load_omp().w4c_gemv_f64(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), M, K, N,
+                             _ptr(y))
+    return y
 
 
 def _load():

@@ -337,3 +337,15 @@ def test_bf16_to_double_matches_torch():
     nan = np.isnan(ref)
     assert np.array_equal(np.isnan(got), nan)
     assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_openmp_baseline_matches_oracle():
+    """The OpenMP CPU baseline spreads the oracle's rows over threads without
+    changing their arithmetic: bit-identical results, ragged shapes included."""
+    from int4_weight_only_w4_gb300 import synthetic as syn
+    assert oracle.omp_threads() >= 1
+    for (M, K, N) in ((1, 128, 1), (3, 256, 17), (8, 1024, 200), (2, 4864, 33)):
+        p = syn.make_problem(f"omp.{M}.{K}.{N}", K, N, M, seed=41)
+        a = oracle.gemv_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N)
+        b = oracle.gemv_f64_omp(p.qweight, p.scales, p.zeros, p.x, M, K, N)
+        assert np.array_equal(a.view(np.uint64), b.view(np.uint64)), (M, K, N)

@@ -39,9 +39,10 @@ def test_bench_imports_the_oracle_only_in_cpu_legs():
     top = [n for n in tree.body if isinstance(n, ast.Import)
            and any(a.name == "oracle" for a in n.names)]
     assert not top, "bench.py imports the oracle at module level"
-    # OracleSampler (and its method next_gemv) serves cpu_baseline and the
-    # reference arm only
-    assert users <= {"OracleSampler", "next_gemv"}, users
+    # OracleSampler (and its methods) serves cpu_baseline and the reference
+    # arm only
+    assert users <= {"OracleSampler", "next_gemv", "per_config", "omp_chain",
+                     "check_outputs"}, users
     callers = set()
     for fn in ast.walk(tree):
         if isinstance(fn, ast.FunctionDef):

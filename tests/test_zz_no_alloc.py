@@ -71,16 +71,17 @@ def test_static_scratch_matches_existing_entry_points(w4):
 
 
 def test_static_scratch_limit_refused_first(w4):
-    # K = 128 and 15 million rows need more counters than the array holds; the
-    # size check runs before the pointer checks, so NULL pointers never launch.
-    need = w4.gemv_workspace_bytes(128, 15_000_000)
+    # Enough rows that the row-block counters alone (4 bytes per 128 rows)
+    # exceed the array, whatever the SM count; the size check runs before the
+    # pointer checks, so NULL pointers never launch.
+    rows = 128 * (w4.STATIC_SCRATCH_BYTES // 4 + 1)
+    need = w4.gemv_workspace_bytes(128, rows)
     assert need > w4.STATIC_SCRATCH_BYTES
     lib = ctypes.CDLL(w4.library_path())
     fn = lib.w4_gemv_ws_static
     fn.restype = ctypes.c_int
     P = ctypes.c_void_p
     fn.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
-    assert fn(None, None, None, None, None, 1, 128, 15_000_000, None) == \
-        w4.Status.SCRATCH_LIMIT
+    assert fn(None, None, None, None, None, 1, 128, rows, None) == w4.Status.SCRATCH_LIMIT
     # a product that fits, with a NULL pointer: refused as an argument error
     assert fn(None, None, None, None, None, 1, 3584, 3584, None) == w4.Status.INVALID_ARG
