@@ -820,10 +820,12 @@ GEMM_MS = (16, 32, 64, 128)
 
 
 def gemm_arm(args):
-    """Per-call timing of w4_gemm (passes of 8 tokens) for M > 8 on the 7B
-    layer shapes: R calls over rotating weight copies in one CUDA graph,
-    median of 5.  One JSON line per (shape, M): effective GB/s against the
-    algorithmic bytes (the weight once), and TFLOP/s (2 M N K)."""
+    """Per-call timing of w4_gemm for M > 8 (the single-pass tensor-core
+    kernel, tiles of up to 128 tokens) on the 7B layer shapes: R calls over
+    rotating weight copies in one CUDA graph, median of 5.  One JSON line per
+    (shape, M): effective GB/s against the algorithmic bytes (the weight
+    once) with its fraction of the measured copy bandwidth, and TFLOP/s
+    (2 M N K) with its fraction of the measured bf16 tensor peak."""
     import torch
 
     from int4_weight_only_w4_gb300 import w4
@@ -831,6 +833,11 @@ def gemm_arm(args):
     torch.cuda.set_device(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     peak, peak_kind = read_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpeak, tpeak_kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        tpeak, tpeak_kind = 1900.0, "fallback"
     stream = torch.cuda.Stream(device=dev)
     for name, K, N in GEMM_SHAPES:
         qw, sc, zp = syn.make_weights(f"{name}.gemm", K, N, SEED, (0.001, 0.02))
@@ -871,11 +878,14 @@ def gemm_arm(args):
                     times.append(e0.elapsed_time(e1) * 1e3 / reps)
             us = statistics.median(times)
             b = canonical_bytes(M, K, N)
+            tflops = 2.0 * M * N * K / us / 1e6
             print(json.dumps({"op": "w4_gemm", "shape": name, "M": M, "K": K, "N": N,
-                              "passes": -(-M // 8), "us_per_call": round(us, 3),
-                              "GBps": round(b / us / 1e3, 1),
+                              "path": "tcgen05", "token_tiles": -(-M // 128),
+                              "us_per_call": round(us, 3), "GBps": round(b / us / 1e3, 1),
                               "frac_of_peak": round(b / us / 1e3 / peak, 4), "peak_kind": peak_kind,
-                              "TFLOPs": round(2.0 * M * N * K / us / 1e6, 2),
+                              "TFLOPs": round(tflops, 2),
+                              "frac_of_tensor_peak": round(tflops / tpeak, 4),
+                              "tensor_peak_kind": tpeak_kind,
                               "tok_per_s": round(M / us * 1e6, 1)}), flush=True)
         del packs, base
         torch.cuda.empty_cache()
@@ -1016,7 +1026,7 @@ def main():
     ap.add_argument("--no-per-shape", action="store_true",
                     help="leave the per-call block out of the default line")
     ap.add_argument("--gemm", action="store_true",
-                    help="per-call timing of w4_gemm (M > 8, passes of 8 tokens)")
+                    help="per-call timing of w4_gemm (M > 8: the tensor-core kernel)")
     ap.add_argument("--swiglu", action="store_true",
                     help="per-call timing of the fused gate/up + SwiGLU product")
     ap.add_argument("--quantize", action="store_true",

@@ -84,21 +84,28 @@ w4_status check_header_common(const void *header, int K, int N, uint32_t layout_
     return W4_OK;
 }
 
-// Passes of at most 8 tokens over the same weight.
+// Up to 8 tokens: the GEMV.  More: one pass over the weight on the tensor
+// cores (w4_gemm_tc.cu), in tiles of 128 tokens.
 w4_status gemm_common(const void *qweight, const void *scales, const void *zeros,
                       const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
                       w4_stream_t stream) {
     if (M < 1) return W4_ERR_UNSUPPORTED;
     if (!valid_kn(K, N)) return W4_ERR_INVALID_ARG;
-    const size_t ybytes = f32_out ? 4 : 2;
-    for (int m0 = 0; m0 < M; m0 += W4_MAX_TOKENS) {
-        const int mp = M - m0 < W4_MAX_TOKENS ? M - m0 : W4_MAX_TOKENS;
-        const w4_status st = gemv_common(
-            qweight, scales, zeros, x + (size_t)m0 * K,
-            static_cast<char *>(y) + (size_t)m0 * N * ybytes, f32_out, mp, K, N, stream);
-        if (st != W4_OK) return st;
-    }
-    return W4_OK;
+    if (M <= W4_MAX_TOKENS) return gemv_common(qweight, scales, zeros, x, y, f32_out, M, K, N,
+                                                stream);
+    if (!qweight || !scales || !zeros || !x || !y) return W4_ERR_INVALID_ARG;
+    if (!aligned(qweight, 16) || !aligned(scales, 16) || !aligned(zeros, 16) ||
+        !aligned(x, 16) || !aligned(y, f32_out ? 4 : 2))
+        return W4_ERR_INVALID_ARG;
+    // tensor-copy coordinates are 32-bit: x rows, and the weight records seen
+    // as 128-byte rows (64 per record)
+    if ((long long)M * K >= (1LL << 40) || (M + 127) / 128 > 65535 ||
+        (long long)w4::row_blocks(N) * (K / 128) * 64 >= (1LL << 31))
+        return W4_ERR_UNSUPPORTED;
+    const int sms = device_sms();
+    if (sms <= 0) return W4_ERR_CUDA;
+    return cuda_status(w4::launch_gemm_tc(qweight, scales, zeros, x, y, f32_out, M, K, N, sms,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 w4_status gemv_swiglu_common(const void *qweight, const void *scales, const void *zeros,

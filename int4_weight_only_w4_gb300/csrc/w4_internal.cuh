@@ -96,6 +96,13 @@ cudaError_t launch_gemv(const void *qweight, const void *scales, const void *zer
                         const GemvShape &shape, int swiglu_I, int num_sms,
                         cudaStream_t stream);
 
+// Tensor-core (tcgen05) product for more than W4_MAX_TOKENS tokens
+// (w4_gemm_tc.cu): one pass over the weight, blocks of 128 rows x 128 tokens.
+int gemm_tc_splits(int K, int N, int num_sms);
+cudaError_t launch_gemm_tc(const void *qweight, const void *scales, const void *zeros,
+                           const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
+                           int num_sms, cudaStream_t stream);
+
 // Workspace path (w4_gemv_sk.cu): grid size, workspace bytes, launch.
 int gemv_ws_blocks(int K, int N, int num_sms);
 size_t gemv_ws_bytes(int K, int N, int num_sms);

@@ -1,6 +1,9 @@
-"""w4_gemm (any M, passes of 8 tokens) through the C ABI: parity with the
-oracle, every row bit-identical to w4_gemv on that token alone, graph capture
-and argument errors."""
+"""w4_gemm (any M) through the C ABI.  Up to 8 tokens it is w4_gemv; more
+tokens run the single-pass tensor-core kernel (tiles of up to 128 tokens, one
+pass over the weight).  Parity with the oracle over several tiles, ragged
+tiles, a single group, K splits and the full-size 7B gate_up and LM head
+(sampled rows); a token's result independent of M and of the other tokens;
+repeatability; graph capture and argument errors."""
 import numpy as np
 import pytest
 
@@ -11,6 +14,10 @@ from tests import w4_testutil as tu
 pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
+
+# The tensor-core kernel splits K over at most 8 blocks of a cluster: the
+# bound's split term uses that maximum.
+TC_MAX_SPLITS = 8
 
 
 @pytest.fixture(scope="module")
@@ -25,49 +32,111 @@ def setup(w4, name, K, N, M, seed):
     return p, w4.pack(qw, sc, zp, K, N), x
 
 
-@pytest.mark.parametrize("M,K,N", [(9, 896, 1000), (16, 3584, 4608), (33, 256, 200),
-                                   (64, 3584, 3584), (17, 18944, 300)])
-def test_gemm_parity(w4, M, K, N):
-    p, packed, x = setup(w4, f"gemm.{M}.{K}.{N}", K, N, M, 1)
+def run(w4, packed, x, M, K, N):
     y32 = torch.empty((M, N), dtype=torch.float32, device="cuda")
     y16 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x, y32, M, K, N)
     w4.gemm(packed.qweight, packed.scales, packed.zeros, x, y16, M, K, N)
     torch.cuda.synchronize()
-    ref, refabs = oracle.gemv_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N, with_abs=True)
-    _, S, fold = w4.gemv_config(K, N)
-    mag = tu.folded_abs(p) if fold else refabs
-    tu.check_gemv(y32.cpu().numpy(), tu.bf16_bits(y16), ref, mag, K, S, f"gemm M={M}",
-                  tu.FOLD_EXTRA_STEPS if fold else 0)
+    return y32, y16
 
 
-def test_gemm_multi_wave_rows_equal_single_token_gemv(w4):
-    """A product of several waves without a K split: passes of 8 and of 4
-    tokens run the persistent grid, the single-token products one block per
-    row block; every row is the same bit for bit."""
-    M, K, N = 20, 1024, 64037
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert w4.gemv_config(K, N)[1] == 1 and (N + 127) // 128 > 3 * sms
-    p, packed, x = setup(w4, "gemm.multiwave", K, N, M, 3)
-    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x, y, M, K, N)
-    for r in (0, 9, 16, 19):
-        one = packed.gemv_f32(x[r:r + 1].contiguous())
-        assert torch.equal(one[0], y[r]), r
+def sample_rows(N, rng, count=1536):
+    if N <= count:
+        return np.arange(N)
+    mid = rng.choice(np.arange(64, N - 64), size=count - 128, replace=False)
+    return np.sort(np.concatenate([np.arange(64), mid, np.arange(N - 64, N)]))
 
 
-def test_gemm_rows_equal_single_token_gemv(w4):
-    M, K, N = 40, 3584, 37888
-    p, packed, x = setup(w4, "gemm.rows", K, N, M, 2)
-    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x, y, M, K, N)
-    for r in (0, 7, 8, 23, 39):
-        one = packed.gemv_f32(x[r:r + 1].contiguous())
-        assert torch.equal(one[0], y[r]), r
-    for m in range(1, 9):                      # M <= 8 is exactly w4_gemv
+# (M, K, N): one and several 128-token tiles with ragged last tiles; one group
+# (K = 128); row counts that are not a multiple of 128; shapes whose K is
+# split over a cluster (few row blocks, long K) and shapes that take more than
+# one wave of blocks (many row blocks).
+TC_CASES = [(9, 896, 1000), (16, 3584, 4608), (17, 18944, 300), (33, 256, 200),
+            (64, 3584, 3584), (128, 896, 1152), (129, 1024, 640), (200, 4864, 896),
+            (300, 128, 256), (40, 1152, 40000)]
+
+
+@pytest.mark.parametrize("M,K,N", TC_CASES)
+def test_gemm_tc_parity(w4, M, K, N):
+    p, packed, x = setup(w4, f"gemm.{M}.{K}.{N}", K, N, M, 1)
+    y32, y16 = run(w4, packed, x, M, K, N)
+    rows = sample_rows(N, np.random.default_rng(7)) if M * N * K > 2 ** 30 else np.arange(N)
+    ref, refabs = oracle.gemv_rows_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N, rows,
+                                       with_abs=True)
+    tu.check_gemv(y32.cpu().numpy()[:, rows], tu.bf16_bits(y16)[:, rows], ref, refabs, K,
+                  TC_MAX_SPLITS, f"gemm M={M} K={K} N={N}")
+
+
+@pytest.mark.parametrize("name,M", [("qwen7b.gate_up", 128), ("qwen7b.down", 96),
+                                    ("qwen7b.lm_head", 64)])
+def test_gemm_tc_full_size_sampled(w4, name, M):
+    """Full-size 7B products (the shapes `bench.py --gemm` times), compared with
+    the oracle on a sample of rows that includes the first and last row blocks."""
+    _, K, N, _, srange = syn.shape(name)
+    p = syn.make_problem(f"{name}.gemm.M{M}", K, N, M, seed=4, scale_range=srange)
+    qw, sc, zp, x = tu.to_device(p)
+    packed = w4.pack(qw, sc, zp, K, N)
+    y32, y16 = run(w4, packed, x, M, K, N)
+    rows = sample_rows(N, np.random.default_rng(11), 1024)
+    ref, refabs = oracle.gemv_rows_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N, rows,
+                                       with_abs=True)
+    tu.check_gemv(y32.cpu().numpy()[:, rows], tu.bf16_bits(y16)[:, rows], ref, refabs, K,
+                  TC_MAX_SPLITS, f"{name} gemm M={M}")
+
+
+@pytest.mark.parametrize("K,N", [(3584, 4608), (18944, 896), (1024, 37888)])
+def test_gemm_tc_token_independent_of_batch(w4, K, N):
+    """A token's fp32 result is the same bit for bit whatever M is and
+    whichever tokens share its tile (the K split depends on K, N and the SM
+    count only; every token column is summed on its own)."""
+    M = 140
+    p, packed, x = setup(w4, f"gemm.inv.{K}.{N}", K, N, M, 5)
+    full = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x, full, M, K, N)
+    for lo, hi in ((0, 9), (0, 128), (128, 140), (5, 30), (100, 140)):
+        m = hi - lo
+        part = torch.empty((m, N), dtype=torch.float32, device="cuda")
+        w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x[lo:hi].contiguous(), part, m,
+                    K, N)
+        torch.cuda.synchronize()
+        assert torch.equal(part, full[lo:hi]), (lo, hi)
+
+
+def test_gemm_tc_repeatable(w4):
+    M, K, N = 77, 18944, 3584
+    p, packed, x = setup(w4, "gemm.rep", K, N, M, 6)
+    first = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x, first, M, K, N)
+    again = torch.empty_like(first)
+    for _ in range(20):
+        w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x, again, M, K, N)
+        torch.cuda.synchronize()
+        assert torch.equal(again, first)
+    w4.check_header(packed.qweight[:128].cpu().numpy().tobytes(), K, N)   # no kernel error
+
+
+def test_gemm_up_to_8_tokens_is_gemv(w4):
+    M, K, N = 8, 3584, 37888
+    p, packed, x = setup(w4, "gemm.le8", K, N, M, 2)
+    for m in range(1, 9):
         a = torch.empty((m, N), dtype=torch.float32, device="cuda")
         w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x[:m].contiguous(), a, m, K, N)
         assert torch.equal(a, packed.gemv_f32(x[:m].contiguous()))
+
+
+def test_gemm_no_write_outside_y(w4):
+    """The tensor-core kernel writes y[M][N] and nothing around it."""
+    M, K, N = 37, 1024, 300
+    p, packed, x = setup(w4, "gemm.guard", K, N, M, 8)
+    pad = 4096
+    buf = torch.full((M * N + 2 * pad,), -7.0, dtype=torch.float32, device="cuda")
+    y = buf[pad:pad + M * N].view(M, N)
+    w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x, y, M, K, N)
+    torch.cuda.synchronize()
+    assert bool((buf[:pad] == -7.0).all()) and bool((buf[pad + M * N:] == -7.0).all())
+    ref = oracle.gemv_f64(p.qweight, p.scales, p.zeros, p.x, M, K, N)
+    assert np.abs(y.cpu().numpy() - ref).max() <= 1e-4 * np.abs(ref).max()
 
 
 def test_gemm_graph_and_errors(w4):
@@ -91,3 +160,8 @@ def test_gemm_graph_and_errors(w4):
     with pytest.raises(w4.W4Error) as e:
         w4.gemm(packed.qweight, packed.scales, packed.zeros, x, y, 0, K, N)
     assert e.value.status == w4.Status.UNSUPPORTED
+    # x must be 16-byte aligned for the tensor copies
+    xs = torch.empty(M * K + 8, dtype=torch.bfloat16, device="cuda")[1:1 + M * K].view(M, K)
+    with pytest.raises(w4.W4Error) as e:
+        w4.gemm(packed.qweight, packed.scales, packed.zeros, xs, y, M, K, N)
+    assert e.value.status == w4.Status.INVALID_ARG
