@@ -839,6 +839,24 @@ def gemm_arm(args):
     except Exception:
         tpeak, tpeak_kind = 1900.0, "fallback"
     stream = torch.cuda.Stream(device=dev)
+    if args.gemm_case:
+        # one shape and M, one weight, eager calls only: the case a profiler captures
+        name, M = args.gemm_case.split(":")
+        M = int(M)
+        K, N = {n: (k, nn) for n, k, nn in GEMM_SHAPES}[name]
+        qw, sc, zp = syn.make_weights(f"{name}.gemm", K, N, SEED, (0.001, 0.02))
+        pw = w4.pack(torch.from_numpy(qw.view(np.int32)).to(dev),
+                     torch.from_numpy(sc.view(np.int16)).to(dev), torch.from_numpy(zp).to(dev),
+                     K, N)
+        x = torch.from_numpy(syn.make_x(f"{name}.gemm.M{M}", M, K, SEED).view(np.int16)) \
+            .to(dev).view(torch.bfloat16)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup + args.steps):
+                w4.gemm(pw.qweight, pw.scales, pw.zeros, x, y, M, K, N, stream=stream)
+        stream.synchronize()
+        print(json.dumps({"gemm_case": name, "M": M, "K": K, "N": N}), flush=True)
+        return 0
     for name, K, N in GEMM_SHAPES:
         qw, sc, zp = syn.make_weights(f"{name}.gemm", K, N, SEED, (0.001, 0.02))
         base = w4.pack(torch.from_numpy(qw.view(np.int32)).to(dev),
@@ -1037,6 +1055,8 @@ def main():
                     help="per-call timing of every workload shape instead of the chain")
     ap.add_argument("--kernel-case", default=None,
                     help="run only this shape's GEMV warmup+steps times (for profilers)")
+    ap.add_argument("--gemm-case", default=None,
+                    help="SHAPE:M -- run only this w4_gemm warmup+steps times (for profilers)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1046,7 +1066,7 @@ def main():
         return quantize_arm(args)
     if args.swiglu:
         return swiglu_arm(args)
-    if args.gemm:
+    if args.gemm or args.gemm_case:
         return gemm_arm(args)
     if args.chain_05b:
         return small_chain_arm(args)
