@@ -5,35 +5,37 @@
 // Passes of 8 tokens ("qengine", section "How the numbers were measured")
 // stream and unpack the weight once per pass; prefill batches need the weight
 // read once.  Here a thread block owns one 128-row block of W and a tile of up
-// to 128 tokens and walks its K groups once, with one role per warp:
+// to 128 tokens and walks its K groups once, with one role per warp (20):
 //   weight producer (warp 0, one lane): per group, the record's 8 KB of
 //     nibbles with one 2-D tensor copy (the record seen as 64 rows of 128 B,
 //     128-byte swizzle, so that the converters' row reads below hit every
 //     bank), plus its 256 B of scales and 64 B of zero points (plain bulk
-//     copies), into a ring of stages;
-//   x producer (warp 18, one lane): per group, the tile's tokens x 128 k of x
+//     copies), into a ring of 12 stages;
+//   x producer (warp 19, one lane): per group, the tile's tokens x 128 k of x
 //     as two 2-D tensor copies of 64 k (128-byte swizzled, K-major: the layout
-//     the tensor cores read), tokens past M filled with zeros by the copy;
+//     the tensor cores read), tokens past M filled with zeros by the copy,
+//     into a ring of 3 to 16 stages (more for smaller tiles);
 //   converters (warps 1..8): warp w owns tensor-memory lanes 32 (w mod 4) ..
-//     +31, i.e. one weight row per thread, and half (w - 1) / 4 of the group's
-//     128 k.  Per group a thread reads its row's 32 nibbles (four 16-byte
-//     loads), forms bf16 (q - z) -- exact: (nibble | 0x4300) read as bf16 is
-//     128 + q, one bf16 add of -(128 + z) -- and writes the 64 values into one
-//     of four operand buffers in tensor memory with one tcgen05.st; the
-//     row's fp32 scale goes to a small ring in shared memory;
-//   issuer (warp 17, one lane): per group, eight tcgen05.mma.kind::f16 with the
-//     weight operand from tensor memory and x from shared memory (M = 128
-//     rows, N = the token tile rounded up to 16, K = 16 each) into one of
-//     two accumulators, then tcgen05.commit to the barriers that free the
-//     operand buffers and publish the sums;
-//   readback (warps 9..16): warp w reads lanes 32 (w mod 4) .. +31 and half
-//     (w - 9) / 4 of the token columns: per group tcgen05.ld of the row's fp32
-//     group sums and acc += s * sum in registers; then the epilogue.
-// A tensor-core instruction of M = 128 rows costs about the same for any N up
-// to 128 (about 100 SM cycles on GB300), so the eight MMAs of a group set the
-// pace for every tile of up to 128 tokens; the other roles run ahead of the
-// issuer (four operand buffers, two accumulators, a 12-record ring) so that
-// it never waits.
+//     +31, i.e. one weight row per thread, and the groups g with g mod 2 ==
+//     (w - 1) / 4.  Per group a thread reads its row's 128 nibbles (eight
+//     16-byte loads, half of each belonging to the row eight below), forms
+//     bf16 (q - z) -- exact: (nibble | 0x4300) read as bf16 is 128 + q, one
+//     bf16 add of -(128 + z) -- and writes the 128 values into one of four
+//     operand buffers in tensor memory (two tcgen05.st); the row's fp32
+//     scale goes to a 16-deep ring in shared memory;
+//   issuers (warps 17, 18, one lane each): the groups alternate between them;
+//     per group eight tcgen05.mma.kind::f16 with the weight operand from
+//     tensor memory and x from shared memory (M = 128 rows, N = the token
+//     tile rounded up to 16, K = 16 each) into one of 2 to 8 accumulators
+//     (32, 64 or 128 columns wide: the tile rounded up), then tcgen05.commit
+//     to the barriers that free the operand buffers and publish the sums.  A
+//     tensor-core instruction holds its issuing thread for about 100 cycles
+//     whatever N is (up to 128), so two issuers on independent accumulators
+//     double the rate;
+//   readback (warps 9..16): warp w reads lanes 32 (w mod 4) .. +31 and the
+//     16-column units u of the token columns with u mod 2 == (w - 9) / 4: per
+//     group tcgen05.ld of the row's fp32 group sums and acc += s * sum in
+//     registers; then the epilogue (or, with a K split, the cluster combine).
 // The group's scale multiplies the group's fp32 sum, exactly the arithmetic of
 // the GEMV's exact path: per group sum_k (q - z) x accumulated in fp32 by the
 // tensor cores, then acc = fma(s, sum, acc) group by group in order.  A
@@ -41,7 +43,7 @@
 //
 // Every wait is bounded (about 2 s of clock cycles): a role that gives up sets
 // the header's error word and the block winds down; the producers wait
-// (bounded) for their copies in flight and the issuer for its last
+// (bounded) for their copies in flight and the issuers for their last
 // tensor-core work before the tensor memory is freed.
 #include <cuda.h>   // CUtensorMap and the tensor-map encoder's types (resolved at run time)
 #include <cuda_bf16.h>
