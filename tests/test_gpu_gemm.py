@@ -54,7 +54,10 @@ def sample_rows(N, rng, count=1536):
 # one wave of blocks (many row blocks).
 TC_CASES = [(9, 896, 1000), (16, 3584, 4608), (17, 18944, 300), (33, 256, 200),
             (64, 3584, 3584), (128, 896, 1152), (129, 1024, 640), (200, 4864, 896),
-            (300, 128, 256), (40, 1152, 40000)]
+            (300, 128, 256), (40, 1152, 40000),
+            # one output row; a few rows under a K split of 8; one group and a
+            # ragged second tile; a tile of exactly 16 tokens past the first
+            (9, 128, 1), (70, 18944, 40), (150, 128, 130), (144, 2048, 2000)]
 
 
 @pytest.mark.parametrize("M,K,N", TC_CASES)
