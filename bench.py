@@ -816,12 +816,13 @@ def swiglu_arm(args):
 
 GEMM_SHAPES = [("qwen7b.qkv", 3584, 4608), ("qwen7b.gate_up", 3584, 37888),
                ("qwen7b.down", 18944, 3584)]
-GEMM_MS = (16, 32, 64, 128)
+GEMM_MS = (16, 17, 32, 64, 128)
 
 
 def gemm_arm(args):
-    """Per-call timing of w4_gemm for M > 8 (the single-pass tensor-core
-    kernel, tiles of up to 128 tokens) on the 7B layer shapes: R calls over
+    """Per-call timing of w4_gemm for M > 8 (up to 16 tokens the GEMV in two
+    passes, beyond that the single-pass tensor-core kernel, tiles of up to
+    128 tokens) on the 7B layer shapes: R calls over
     rotating weight copies in one CUDA graph, median of 5.  One JSON line per
     (shape, M): effective GB/s against the algorithmic bytes (the weight
     once) with its fraction of the measured copy bandwidth, and TFLOP/s
@@ -898,7 +899,8 @@ def gemm_arm(args):
             b = canonical_bytes(M, K, N)
             tflops = 2.0 * M * N * K / us / 1e6
             print(json.dumps({"op": "w4_gemm", "shape": name, "M": M, "K": K, "N": N,
-                              "path": "tcgen05", "token_tiles": -(-M // 128),
+                              "path": "gemv_passes_of_8" if M <= 16 else "tcgen05",
+                              "token_tiles": -(-M // 128),
                               "us_per_call": round(us, 3), "GBps": round(b / us / 1e3, 1),
                               "frac_of_peak": round(b / us / 1e3 / peak, 4), "peak_kind": peak_kind,
                               "TFLOPs": round(tflops, 2),

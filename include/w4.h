@@ -163,27 +163,30 @@ w4_status w4_gemv_f32(const void *qweight, const void *scales, const void *zeros
                       w4_stream_t stream);
 
 /*
- * The product for any number of tokens M >= 1.  Up to 8 tokens it is w4_gemv
- * (same kernel, same bits).  For more tokens the weight is read once, in one
- * pass on the tensor cores, where passes of 8 tokens ("qengine", section "How
- * the numbers were measured") would stream it once per pass: a thread block
- * owns a 128-row block of W and a tile of up to 128 tokens; per 128-k group
- * it unpacks (q - z) exactly to bf16 into tensor memory, multiplies it by the
- * tile's x on the tensor cores with fp32 accumulation, and adds s times the
- * group's sum into the token's fp32 result, group by group in order (the
- * arithmetic of the GEMV's exact path).  A token's result does not depend on
- * M or on which tokens share its tile, and repeated calls give the same bits;
- * rows for M > 8 are not bit-identical to w4_gemv's (different summation
- * order inside a group), both lying within the stated tolerances of the
- * oracle.  Long K with few row blocks is split over up to 8 blocks of a
- * thread-block cluster, combined in a fixed order.
+ * The product for any number of tokens M >= 1.  Up to 16 tokens it is w4_gemv
+ * in passes of at most 8 tokens (one or two passes over the weight; row m is
+ * bit-identical to w4_gemv on that token alone).  For more tokens the weight
+ * is read once, in one pass on the tensor cores, where passes of 8 tokens
+ * ("qengine", section "How the numbers were measured") would stream it once
+ * per pass: a thread block owns a 128-row block of W and a tile of up to 128
+ * tokens; per 128-k group it unpacks (q - z) exactly to bf16 into tensor
+ * memory, multiplies it by the tile's x on the tensor cores with fp32
+ * accumulation, and adds s times the group's sum into the token's fp32
+ * result, group by group in order (the arithmetic of the GEMV's exact path).
+ * There a token's result does not depend on M (> 16) or on which tokens share
+ * its tile, and repeated calls give the same bits; its rows are not
+ * bit-identical to w4_gemv's (different summation order inside a group), both
+ * lying within the stated tolerances of the oracle.  Long K with few row
+ * blocks is split over up to 8 blocks of a thread-block cluster, combined in
+ * a fixed order.
  *   qweight, scales, zeros, y [M][N], stream : as for w4_gemv
- *   x [M][K]  : as for w4_gemv; for M > 8 read with tensor copies, so its
+ *   x [M][K]  : as for w4_gemv; for M > 16 read with tensor copies, so its
  *               address must be 16-byte aligned
- * The kernel may write the header's error word (byte offset 28), as w4_gemv.
- * Errors: W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED (M < 1, or M * K >= 2^40, or
- * more than 65535 tiles of 128 tokens, or a weight of 2^25 or more 128 x 128
- * records), W4_ERR_CUDA.
+ * The kernels may write the header's error word (byte offset 28), as w4_gemv.
+ * Errors: W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED (M < 1, or for M > 16:
+ * M * K >= 2^40, more than 65535 tiles of 128 tokens, or a weight of 2^25 or
+ * more 128 x 128 records), W4_ERR_CUDA; in passes, the first error stops the
+ * rest.
  */
 w4_status w4_gemm(const void *qweight, const void *scales, const void *zeros, const uint16_t *x,
                   uint16_t *y, int M, int K, int N, w4_stream_t stream);

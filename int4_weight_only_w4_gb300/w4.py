@@ -172,8 +172,8 @@ def gemv_f32(qweight, scales, zeros, x, y, M: int, K: int, N: int, stream=None) 
 
 
 def gemm(qweight, scales, zeros, x, y, M: int, K: int, N: int, stream=None) -> None:
-    """w4_gemm: y[M, N] (bfloat16) for any M >= 1 (M <= 8: w4_gemv; more: one
-    tensor-core pass over the weight)."""
+    """w4_gemm: y[M, N] (bfloat16) for any M >= 1 (M <= 16: w4_gemv in passes
+    of 8; more: one tensor-core pass over the weight)."""
     _ok(_gemm(_ptr(qweight), _ptr(scales), _ptr(zeros), _ptr(x), _ptr(y), M, K, N,
               _stream(stream, x)), "w4_gemm")
 

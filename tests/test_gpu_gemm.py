@@ -1,7 +1,8 @@
-"""w4_gemm (any M) through the C ABI.  Up to 8 tokens it is w4_gemv; more
-tokens run the single-pass tensor-core kernel (tiles of up to 128 tokens, one
-pass over the weight).  Parity with the oracle over several tiles, ragged
-tiles, a single group, K splits and the full-size 7B gate_up and LM head
+"""w4_gemm (any M) through the C ABI.  Up to 16 tokens it is w4_gemv in
+passes of 8 (each row the single-token product, bit for bit); more tokens run
+the single-pass tensor-core kernel (tiles of up to 128 tokens, one pass over
+the weight).  Parity with the oracle over several tiles, ragged tiles, a
+single group, K splits and the full-size 7B gate_up, down and LM head
 (sampled rows); a token's result independent of M and of the other tokens;
 repeatability; graph capture and argument errors."""
 import numpy as np
@@ -52,12 +53,12 @@ def sample_rows(N, rng, count=1536):
 # (K = 128); row counts that are not a multiple of 128; shapes whose K is
 # split over a cluster (few row blocks, long K) and shapes that take more than
 # one wave of blocks (many row blocks).
-TC_CASES = [(9, 896, 1000), (16, 3584, 4608), (17, 18944, 300), (33, 256, 200),
+TC_CASES = [(17, 896, 1000), (24, 3584, 4608), (17, 18944, 300), (33, 256, 200),
             (64, 3584, 3584), (128, 896, 1152), (129, 1024, 640), (200, 4864, 896),
             (300, 128, 256), (40, 1152, 40000),
             # one output row; a few rows under a K split of 8; one group and a
             # ragged second tile; a tile of exactly 16 tokens past the first
-            (9, 128, 1), (70, 18944, 40), (150, 128, 130), (144, 2048, 2000)]
+            (20, 128, 1), (70, 18944, 40), (150, 128, 130), (144, 2048, 2000)]
 
 
 @pytest.mark.parametrize("M,K,N", TC_CASES)
@@ -97,7 +98,7 @@ def test_gemm_tc_token_independent_of_batch(w4, K, N):
     p, packed, x = setup(w4, f"gemm.inv.{K}.{N}", K, N, M, 5)
     full = torch.empty((M, N), dtype=torch.float32, device="cuda")
     w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x, full, M, K, N)
-    for lo, hi in ((0, 9), (0, 128), (128, 140), (5, 30), (100, 140)):
+    for lo, hi in ((0, 17), (0, 128), (120, 140), (5, 30), (100, 140)):
         m = hi - lo
         part = torch.empty((m, N), dtype=torch.float32, device="cuda")
         w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x[lo:hi].contiguous(), part, m,
@@ -119,13 +120,21 @@ def test_gemm_tc_repeatable(w4):
     w4.check_header(packed.qweight[:128].cpu().numpy().tobytes(), K, N)   # no kernel error
 
 
-def test_gemm_up_to_8_tokens_is_gemv(w4):
-    M, K, N = 8, 3584, 37888
-    p, packed, x = setup(w4, "gemm.le8", K, N, M, 2)
-    for m in range(1, 9):
+def test_gemm_up_to_16_tokens_is_gemv_in_passes(w4):
+    M, K, N = 16, 3584, 37888
+    p, packed, x = setup(w4, "gemm.le16", K, N, M, 2)
+    for m in range(1, 17):
         a = torch.empty((m, N), dtype=torch.float32, device="cuda")
         w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x[:m].contiguous(), a, m, K, N)
-        assert torch.equal(a, packed.gemv_f32(x[:m].contiguous()))
+        # pass 1: tokens 0..7, pass 2: tokens 8..m-1, each exactly w4_gemv
+        assert torch.equal(a[:8], packed.gemv_f32(x[:min(m, 8)].contiguous()))
+        if m > 8:
+            assert torch.equal(a[8:], packed.gemv_f32(x[8:m].contiguous()))
+    # and each row is the single-token product
+    a = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    w4.gemm_f32(packed.qweight, packed.scales, packed.zeros, x, a, M, K, N)
+    for r in (0, 7, 8, 15):
+        assert torch.equal(a[r], packed.gemv_f32(x[r:r + 1].contiguous())[0]), r
 
 
 def test_gemm_no_write_outside_y(w4):
