@@ -1,4 +1,4 @@
-// w4_gemm for more than 8 tokens: one pass over the weight on the 5th-generation
+// w4_gemm for more than 16 tokens: one pass over the weight on the 5th-generation
 // tensor cores (tcgen05: accumulators and the dequantised weight operand in
 // tensor memory).
 //
