@@ -183,6 +183,9 @@ w4_status w4_gemv_f32(const void *qweight, const void *scales, const void *zeros
  *   x [M][K]  : as for w4_gemv; for M > 16 read with tensor copies, so its
  *               address must be 16-byte aligned
  * The kernels may write the header's error word (byte offset 28), as w4_gemv.
+ * For M > 16 every thread block takes all of its SM's tensor memory while it
+ * runs: a kernel on another stream holding tensor memory on the same SM
+ * delays it until that memory is freed.
  * Errors: W4_ERR_INVALID_ARG, W4_ERR_UNSUPPORTED (M < 1, or for M > 16:
  * M * K >= 2^40, more than 65535 tiles of 128 tokens, or a weight of 2^25 or
  * more 128 x 128 records), W4_ERR_CUDA; in passes, the first error stops the
