@@ -1,5 +1,5 @@
 /*
- * w4_cpu_omp.c -- CPU BASELINE for timing only (not a checker).
+ * w4_cpu_omp.c -- the all-core CPU baseline, for timing only (not a checker).
  *
  * The oracle's matrix-vector product (w4_oracle.c) restated with its output
  * rows shared among all host cores (OpenMP), so that the GPU can be reported
