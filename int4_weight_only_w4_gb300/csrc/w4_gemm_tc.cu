@@ -197,6 +197,19 @@ __device__ __forceinline__ void tc_ld16_pair(uint32_t taddr, float (&v)[16], flo
     }
 }
 
+// (a0, a1) = fma(s, (v0, v1), (a0, a1)) as one packed instruction: each lane
+// is the IEEE fused multiply-add rounded to nearest, the same bits as fmaf.
+__device__ __forceinline__ void fma2(float &a0, float &a1, float s, float v0, float v1) {
+    asm("{\n\t.reg .b64 a, b, c;\n\t"
+        "mov.b64 a, {%0, %1};\n\t"
+        "mov.b64 b, {%2, %2};\n\t"
+        "mov.b64 c, {%3, %4};\n\t"
+        "fma.rn.f32x2 a, b, c, a;\n\t"
+        "mov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(s), "f"(v0), "f"(v1));
+}
+
 // This thread's 32 words into 32 consecutive columns of its tensor-memory lane.
 __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
@@ -482,15 +495,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__
                     float v[16], u[16];
                     tc_ld16_pair(t_acc + (uint32_t)(d * dcols + 32 * l), v, u);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        acc[16 * l + i] = fmaf(s_g, v[i], acc[16 * l + i]);
-                        acc[16 * (l + 1) + i] = fmaf(s_g, u[i], acc[16 * (l + 1) + i]);
+                    for (int i = 0; i < 16; i += 2) {
+                        fma2(acc[16 * l + i], acc[16 * l + i + 1], s_g, v[i], v[i + 1]);
+                        fma2(acc[16 * (l + 1) + i], acc[16 * (l + 1) + i + 1], s_g, u[i],
+                             u[i + 1]);
                     }
                 } else if (16 * (2 * l + half) < n_mma) {
                     float v[16];
                     tc_ld16(t_acc + (uint32_t)(d * dcols + 32 * l), v);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[16 * l + i] = fmaf(s_g, v[i], acc[16 * l + i]);
+                    for (int i = 0; i < 16; i += 2)
+                        fma2(acc[16 * l + i], acc[16 * l + i + 1], s_g, v[i], v[i + 1]);
                 }
             }
             tc_fence_before();
