@@ -89,6 +89,29 @@ def test_gemv_argument_errors(lib, kw, want):
     assert gemv(lib, **kw) == want
 
 
+def gemm(lib, q=FAKE, s=FAKE, z=FAKE, x=FAKE, y=FAKE, M=17, K=128, N=16):
+    lib.w4_gemm.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+    return lib.w4_gemm(q, s, z, x, y, M, K, N, None)
+
+
+# w4_gemm above 16 tokens (the tensor-core path): every case fails validation
+# before the device is touched.  1 = W4_ERR_INVALID_ARG, 2 = W4_ERR_UNSUPPORTED.
+@pytest.mark.parametrize("kw,want", [
+    (dict(M=0), 2), (dict(M=-3), 2), (dict(K=100), 1), (dict(N=0), 1),
+    (dict(q=None), 1), (dict(s=None), 1), (dict(z=None), 1), (dict(x=None), 1),
+    (dict(y=None), 1), (dict(q=FAKE + 8), 1), (dict(s=FAKE + 4), 1), (dict(z=FAKE + 8), 1),
+    (dict(x=FAKE + 8), 1), (dict(y=FAKE + 1), 1),
+    # more than 65535 tiles of 128 tokens
+    (dict(M=65536 * 128 + 1, K=128), 2),
+    # M * K >= 2^40
+    (dict(M=1 << 22, K=1 << 18), 2),
+    # a weight of 2^25 or more 128 x 128 records (tensor-copy rows past 2^31)
+    (dict(M=17, K=128 * 1024, N=32768 * 128), 2),
+])
+def test_gemm_argument_errors(lib, kw, want):
+    assert gemm(lib, **kw) == want
+
+
 def test_gemv_ws_argument_errors(lib):
     lib.w4_gemv_ws.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
                                ctypes.c_size_t, P]
