@@ -606,16 +606,70 @@ EncodeTiledFn encode_tiled() {
 
 }  // namespace
 
+namespace {
+
+std::atomic<bool> g_attr_done[2][64] = {};
+
+// The kernel's dynamic shared memory limit, set once per device and variant.
+cudaError_t prepare_tc(bool f32_out, int dev) {
+    if (g_attr_done[f32_out][dev].load(std::memory_order_acquire)) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(
+        f32_out ? gemm_tc_kernel<true> : gemm_tc_kernel<false>,
+        cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::alloc);
+    if (e == cudaSuccess) g_attr_done[f32_out][dev].store(true, std::memory_order_release);
+    return e;
+}
+
+// How many clusters of s blocks of the kernel can be resident at once on the
+// device (clusters are placed whole, within one GPC); cached per device and
+// size, 0 when the query fails.
+std::atomic<int> g_max_clusters[64][9] = {};
+
+int max_active_clusters(int dev, int s) {
+    int n = g_max_clusters[dev][s].load(std::memory_order_acquire);
+    if (n != 0) return n > 0 ? n : 0;
+    n = -1;
+    if (prepare_tc(false, dev) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, (unsigned)s);
+        cfg.blockDim = dim3(kTcThreads, 1, 1);
+        cfg.dynamicSmemBytes = TcSmem::alloc;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = (unsigned)s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int q = 0;
+        if (cudaOccupancyMaxActiveClusters(&q, (const void *)gemm_tc_kernel<false>, &cfg) ==
+                cudaSuccess &&
+            q > 0)
+            n = q;
+        else
+            (void)cudaGetLastError();   // clear the error the failed query left
+    }
+    g_max_clusters[dev][s].store(n, std::memory_order_release);
+    return n > 0 ? n : 0;
+}
+
+}  // namespace
+
 int gemm_tc_splits(int K, int N, int num_sms) {
-    // The largest of 1, 2, 4, 8 that keeps one block per row block and split
-    // within one wave (one block per SM) and leaves each block at least four
-    // groups.  It depends on K, N and the SM count only, never on M, so a
-    // token's result is the same whatever M is.
+    // The largest S of 1..8 that gives every block at least four groups and
+    // keeps the row blocks' clusters of S blocks within one wave (one block
+    // per SM; as many clusters resident as there are row blocks).  It
+    // depends on K, N and the device only, never on M, so a token's result
+    // is the same whatever M is.
     const int NB = row_blocks(N), G = K / kGroup;
-    int S = 1;
-    while (S < 8 && (long long)NB * (2 * S) <= (num_sms > 0 ? num_sms : 1) && G >= 4 * (2 * S))
-        S *= 2;
-    return S;
+    int smax = num_sms > 0 ? num_sms / NB : 1;
+    if (smax > 8) smax = 8;
+    if (smax > G / 4) smax = G / 4;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    for (int S = smax; S >= 2; --S)
+        if (max_active_clusters(dev, S) >= NB) return S;
+    return 1;
 }
 
 // Tokens per x tile copy: 128, or M rounded up to 16 when M is smaller.
@@ -626,7 +680,6 @@ int gemm_tc_x_rows(int M) {
 cudaError_t launch_gemm_tc(const void *qweight, const void *scales, const void *zeros,
                            const uint16_t *x, void *y, bool f32_out, int M, int K, int N,
                            int num_sms, cudaStream_t stream) {
-    static std::atomic<bool> attr_done[2][64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -634,12 +687,7 @@ cudaError_t launch_gemm_tc(const void *qweight, const void *scales, const void *
     const EncodeTiledFn encode = encode_tiled();
     if (!encode) return cudaErrorNotSupported;
     auto kern = f32_out ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
-    if (!attr_done[f32_out][dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TcSmem::alloc);
-        if (e != cudaSuccess) return e;
-        attr_done[f32_out][dev].store(true, std::memory_order_release);
-    }
+    if ((e = prepare_tc(f32_out, dev)) != cudaSuccess) return e;
     const int NB = row_blocks(N), Gall = K / kGroup;
     const int xrows = gemm_tc_x_rows(M);
     const char *q = static_cast<const char *>(qweight);
