@@ -88,8 +88,8 @@ w4_status check_header_common(const void *header, int K, int N, uint32_t layout_
 // the weight; each row bit-identical to the single-token GEMV).  More: one
 // pass over the weight on the tensor cores (w4_gemm_tc.cu), in tiles of 128
 // tokens.  Measured on the 7B shapes: two passes for 16 tokens against the
-// tensor cores for 17, gate_up 32.0 vs 44.1 us, down 24.6 vs 27.8, qkv 9.6 vs
-// 10.4; a third pass (17-24 tokens) would cost about 47, 37 and 14 us.
+// tensor cores for 17, gate_up 32.0 vs 44.0 us, qkv 9.5 vs 10.4, down 24.6 vs
+// 24.3 (even); a third pass (17-24 tokens) would cost about 47, 14 and 37 us.
 constexpr int kGemmPassMaxTokens = 2 * W4_MAX_TOKENS;
 
 w4_status gemm_common(const void *qweight, const void *scales, const void *zeros,
