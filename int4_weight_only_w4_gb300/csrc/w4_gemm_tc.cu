@@ -622,12 +622,13 @@ cudaError_t prepare_tc(bool f32_out, int dev) {
 
 // How many clusters of s blocks of the kernel can be resident at once on the
 // device (clusters are placed whole, within one GPC); cached per device and
-// size, 0 when the query fails.
+// size, -1 when the query failed (also cached, so that a device's choice
+// never changes between calls).
 std::atomic<int> g_max_clusters[64][9] = {};
 
 int max_active_clusters(int dev, int s) {
     int n = g_max_clusters[dev][s].load(std::memory_order_acquire);
-    if (n != 0) return n > 0 ? n : 0;
+    if (n != 0) return n;
     n = -1;
     if (prepare_tc(false, dev) == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
@@ -650,7 +651,7 @@ int max_active_clusters(int dev, int s) {
             (void)cudaGetLastError();   // clear the error the failed query left
     }
     g_max_clusters[dev][s].store(n, std::memory_order_release);
-    return n > 0 ? n : 0;
+    return n;
 }
 
 }  // namespace
@@ -658,17 +659,19 @@ int max_active_clusters(int dev, int s) {
 int gemm_tc_splits(int K, int N, int num_sms) {
     // The largest S of 1..8 that gives every block at least four groups and
     // keeps the row blocks' clusters of S blocks within one wave (one block
-    // per SM; as many clusters resident as there are row blocks).  It
-    // depends on K, N and the device only, never on M, so a token's result
-    // is the same whatever M is.
+    // per SM; as many clusters resident as there are row blocks; where the
+    // runtime cannot tell, powers of two only).  It depends on K, N and the
+    // device only, never on M, so a token's result is the same whatever M is.
     const int NB = row_blocks(N), G = K / kGroup;
     int smax = num_sms > 0 ? num_sms / NB : 1;
     if (smax > 8) smax = 8;
     if (smax > G / 4) smax = G / 4;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-    for (int S = smax; S >= 2; --S)
-        if (max_active_clusters(dev, S) >= NB) return S;
+    for (int S = smax; S >= 2; --S) {
+        const int n = max_active_clusters(dev, S);
+        if (n < 0 ? (S & (S - 1)) == 0 : n >= NB) return S;
+    }
     return 1;
 }
 
